@@ -1,0 +1,410 @@
+"""Benchmark of the USP attention hot path (one JSON line on rank 0).
+
+A step is one full pass of the path over one synthetic batch:
+  pad/shard Q,K,V -> seq->head all-to-all with RoPE (Q,K) and plain (V)
+  -> causal GQA attention forward -> head->seq (O)
+  -> pad/shard dO -> seq->head (dO) -> attention backward
+  -> head->seq (dQ, dK with inverse RoPE; dV).
+The default workload is the 120 000-token SP8 layer (Hq/Hkv/D = 32/8/128,
+YaRN RoPE to 131 072).  Inputs (0.98 GB for Q alone) are larger than L2, so
+no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU fp64 oracle, timed
+
+Multi-GPU runs (torchrun, one rank per GPU) are independent replicas: the
+path has no cross-GPU step here, so every rank runs the same workload and
+`value` is the tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "USP attn fwd+bwd tokens/s and TFLOP/s (% bf16 peak); repack GB/s (% HBM)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            out = {}
+            for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                v = d.get(k)
+                if isinstance(v, dict):
+                    v = v.get("value")
+                if isinstance(v, (int, float)):
+                    out[k] = float(v)
+            if "hbm_gbs" in out and "bf16_tflops" in out:
+                out.setdefault("bf16_tflops_sustained", out["bf16_tflops"])
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def causal_pairs(S, cu):
+    if cu is None:
+        return S * (S + 1) // 2
+    lens = np.diff(np.asarray(cu, np.int64))
+    return int((lens * (lens + 1) // 2).sum())
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id=None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_bus_id(torch):
+    try:
+        p = torch.cuda.get_device_properties(torch.cuda.current_device())
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl, inp, target_s, fixed_rows=None):
+    """Time the oracle's forward+backward of query head 0 (and its KV head)
+    on the first S' rows, S' grown until one run takes about target_s
+    seconds (or S' = fixed_rows).  Returns (seconds, S', scale factor to the
+    full workload)."""
+    from oracle import usp_oracle as O
+    D = wl.D
+    scale = 1.0 / math.sqrt(D)
+    cos, sin = O.rope_cos_sin(max(wl.table_len, wl.S), D, wl.rope_base, wl.yarn_factor,
+                              wl.yarn_orig_ctx)
+    Sp = fixed_rows or 512
+    while True:
+        Sp = min(Sp, wl.S)
+        q = O.bf16_to_f64(inp.q[:Sp, :1])
+        k = O.bf16_to_f64(inp.k[:Sp, :1])
+        v = O.bf16_to_f64(inp.v[:Sp, :1])
+        do = O.bf16_to_f64(inp.do[:Sp, :1])
+        cu = None
+        if inp.cu is not None:
+            cu = np.concatenate([inp.cu[inp.cu < Sp], [Sp]]).astype(np.int64)
+        t0 = time.perf_counter()
+        O.full_sequence(q, k, v, do, cu, cos, sin, scale)
+        dt = time.perf_counter() - t0
+        if fixed_rows or dt >= target_s / 3 or Sp >= wl.S:
+            break
+        Sp = int(Sp * min(4.0, max(1.3, math.sqrt(target_s / max(dt, 1e-3)))))
+    pairs_s = causal_pairs(Sp, cu)
+    pairs_f = causal_pairs(wl.S, inp.cu)
+    factor = (pairs_f * wl.Hq) / pairs_s
+    return dt, Sp, factor
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl, inp):
+    """--impl reference: the oracle, timed on host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    times = []
+    _, Sp, factor = oracle_sample(wl, inp, args.ref_seconds)
+    for i in range(args.warmup + args.steps):
+        dt, Sp, factor = oracle_sample(wl, inp, args.ref_seconds, fixed_rows=Sp)
+        if i >= args.warmup:
+            times.append(dt * factor)
+    full_s = statistics.median(times)
+    value = wl.S / full_s
+    sample = (f"oracle fwd+bwd of q head 0 / kv head 0 on the first {Sp} rows, "
+              f"scaled by causal pairs x heads ({factor:.4g}x) to the full workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": full_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "S": wl.S, "P": wl.P, "Hq": wl.Hq, "Hkv": wl.Hkv,
+                   "D": wl.D},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_usp(args, wl, inp):
+    import torch
+    import torch.distributed as dist
+    from ulysses_sequence_attention_usp_gb300 import build as _build
+    _build.build()
+    from ulysses_sequence_attention_usp_gb300 import binding as B
+    from ulysses_sequence_attention_usp_gb300.pipeline import UlyssesAttention
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                          rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
+                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev)
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    st = torch.cuda.current_stream(dev)
+    d = ua.dims
+
+    # staged step with events between the calls (all on `st`)
+    stage_names = ["pad_qkv", "repack_qkv", "attn_fwd", "repack_o", "pad_do", "repack_do",
+                   "attn_bwd", "repack_grads"]
+
+    def step(ev=None):
+        mark = (lambda i: ev[i].record(st)) if ev is not None else (lambda i: None)
+        mark(0)
+        B.usp_pad_shard(d, q, wl.Hq, ua.q_seq, ua.pos, ua.doc, st)
+        B.usp_pad_shard(d, k, wl.Hkv, ua.k_seq, None, None, st)
+        B.usp_pad_shard(d, v, wl.Hkv, ua.v_seq, None, None, st)
+        mark(1)
+        B.usp_seq_to_head_rope(d, ua.q_seq, wl.Hq, ua.pos, ua.rope, ua.rope_len, 1, ua.q_h, st)
+        B.usp_seq_to_head_rope(d, ua.k_seq, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1, ua.k_h, st)
+        B.usp_seq_to_head_rope(d, ua.v_seq, wl.Hkv, None, None, 0, 0, ua.v_h, st)
+        mark(2)
+        B.usp_attn_fwd(d, ua.q_h, ua.k_h, ua.v_h, ua.doc, ua.o_h, ua.lse, st)
+        mark(3)
+        B.usp_head_to_seq(d, ua.o_h, wl.Hq, None, None, 0, 0, ua.o, st)
+        mark(4)
+        B.usp_pad_shard(d, do, wl.Hq, ua.do_seq, None, None, st)
+        mark(5)
+        B.usp_seq_to_head_rope(d, ua.do_seq, wl.Hq, None, None, 0, 0, ua.do_h, st)
+        mark(6)
+        B.usp_attn_bwd(d, ua.q_h, ua.k_h, ua.v_h, ua.o_h, ua.lse, ua.do_h, ua.doc, ua.dq_h,
+                       ua.dk_h, ua.dv_h, ua.ws, ua.ws_bytes, st)
+        mark(7)
+        B.usp_head_to_seq(d, ua.dq_h, wl.Hq, ua.pos, ua.rope, ua.rope_len, -1, ua.dq, st)
+        B.usp_head_to_seq(d, ua.dk_h, wl.Hkv, ua.pos, ua.rope, ua.rope_len, -1, ua.dk, st)
+        B.usp_head_to_seq(d, ua.dv_h, wl.Hkv, None, None, 0, 0, ua.dv, st)
+        mark(8)
+
+    for _ in range(args.warmup):
+        step()
+    ua.check(st)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_bus_id(torch))
+    clocks.start()
+    barrier()
+    n0 = B.usp_launch_count()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(st)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(st)
+    barrier()
+    launches = B.usp_launch_count() - n0
+    clk = clocks.stop()
+    ua.check(st)
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    stage_ms = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, n in enumerate(stage_names)}
+    if world > 1:
+        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed = float(tt.item())
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory()  # noqa: E731
+    hq_, hk_, hv_, hdo_ = pin(inp.q), pin(inp.k), pin(inp.v), pin(inp.do)
+    outs = [torch.empty(t.shape, dtype=torch.int16).pin_memory()
+            for t in (ua.o, ua.dq, ua.dk, ua.dv)]
+
+    def e2e_step():
+        for src, dst in ((hq_, q), (hk_, k), (hv_, v), (hdo_, do)):
+            dst.view(torch.int16).copy_(src, non_blocking=True)
+        ua.step(q, k, v, do, st)
+        for src, dst in zip((ua.o, ua.dq, ua.dk, ua.dv), outs):
+            dst.copy_(src.view(torch.int16), non_blocking=True)
+
+    e2e_step()
+    barrier()
+    a_ev = torch.cuda.Event(enable_timing=True)
+    b_ev = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 3))
+    a_ev.record(st)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b_ev.record(st)
+    barrier()
+    ua.check(st)
+    e2e_t = a_ev.elapsed_time(b_ev) / 1e3
+    if world > 1:
+        tt = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_t = float(tt.item())
+    h2d = sum(a.nbytes for a in (inp.q, inp.k, inp.v, inp.do))
+    d2h = sum(t.numel() * 2 for t in (ua.o, ua.dq, ua.dk, ua.dv))
+
+    if rank == 0:
+        peaks, src = load_peaks()
+        pairs = causal_pairs(wl.S, inp.cu)
+        f_fwd = 4.0 * wl.D * wl.Hq * pairs
+        f_bwd = 10.0 * wl.D * wl.Hq * pairs
+        step_s = elapsed / args.steps
+        value = world * wl.S * args.steps / elapsed
+        t_fwd = stage_ms["attn_fwd"] / 1e3
+        t_bwd = stage_ms["attn_bwd"] / 1e3
+        bq = wl.S_pad * wl.Hq * wl.D * 2
+        bkv = wl.S_pad * wl.Hkv * wl.D * 2
+        tab = wl.S_pad * wl.D * 4                  # one (cos, sin) row per position
+        rep_bytes = {"repack_qkv": 2 * (bq + 2 * bkv) + 2 * tab, "repack_o": 2 * bq,
+                     "repack_do": 2 * bq, "repack_grads": 2 * (bq + 2 * bkv) + 2 * tab}
+        rep_t = sum(stage_ms[n] for n in rep_bytes) / 1e3
+        rep_gbs = sum(rep_bytes.values()) / rep_t / 1e9
+        peak_t = peaks["bf16_tflops_sustained"]
+        bwd_tf = f_bwd / t_bwd / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "S": wl.S, "P": wl.P, "Hq": wl.Hq, "Hkv": wl.Hkv,
+                       "D": wl.D, "rope": ("yarn x%g to %d" % (wl.yarn_factor, wl.rope_len)
+                                           if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
+                       "parallelism": f"replicas x{world} (P={wl.P} virtual shards per GPU)",
+                       "l2": "inputs larger than L2 (Q alone %.2f GB); no flush" % (bq / 1e9)},
+            "roofline": {"kernel": "usp_attn_bwd", "bound": "tensor", "achieved": bwd_tf,
+                         "peak": peak_t, "unit": "TFLOP/s", "frac": bwd_tf / peak_t,
+                         "traffic": None, "peak_source": f"{src} (sustained bf16)",
+                         "flops_per_launch": f_bwd},
+            "attention": {"fwd_tflops": f_fwd / t_fwd / 1e12, "bwd_tflops": bwd_tf,
+                          "fwd_frac": f_fwd / t_fwd / 1e12 / peak_t,
+                          "fwd_bwd_tflops": (f_fwd + f_bwd) / (t_fwd + t_bwd) / 1e12,
+                          "fwd_ms": t_fwd * 1e3, "bwd_ms": t_bwd * 1e3,
+                          "causal_pairs": pairs},
+            "repack": {"gbps": rep_gbs, "frac": rep_gbs / peaks["hbm_gbs"],
+                       "peak_gbps": peaks["hbm_gbs"], "peak_source": src,
+                       "bytes_per_step": sum(rep_bytes.values())},
+            "stage_ms": stage_ms,
+            "gpu_launches": launches,
+            "e2e": {"value": world * wl.S * e2e_steps / e2e_t, "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "clocks": clk,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            dt, Sp, factor = oracle_sample(wl, inp, args.cpu_seconds)
+            line["cpu_baseline"] = {
+                "value": wl.S / (dt * factor), "unit": "tokens/s", "cores": cpu_cores(),
+                "kind": "oracle",
+                "sample": (f"oracle fwd+bwd of q head 0 / kv head 0 on the first {Sp} rows "
+                           f"({dt:.1f} s), scaled by causal pairs x heads ({factor:.4g}x)")}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
+    ap.add_argument("--workload", default="sp8_120k")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, make_inputs
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference" and int(os.environ.get("RANK", "0")) != 0:
+        return
+    inp = make_inputs(wl, 0)
+    if args.impl == "reference":
+        run_reference(args, wl, inp)
+    else:
+        run_usp(args, wl, inp)
+
+
+if __name__ == "__main__":
+    main()

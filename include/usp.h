@@ -1,0 +1,210 @@
+/*
+ * usp.h -- C ABI of the GB300-native Ulysses sequence-parallel (USP)
+ * attention hot path.
+ *
+ * What the calls compute (sources: SpecForge PR #728 "feat(dspark): add
+ * Ulysses sequence parallel training", sections Modifications and Accuracy
+ * Test; basetenlabs/Megatron-LM PR #7 "GLM-5.2 131k context parallelism",
+ * section Purpose; zhtmike/verl PR #45 "[trainer] feat: support sequence
+ * parallel"):
+ *
+ *   A sequence of S tokens (one document, or packed documents described by
+ *   cu_seqlens) is padded to S_pad = ceil(S/P)*P rows and split into P
+ *   contiguous shards of S_loc = S_pad/P rows, one per Ulysses rank.  The P
+ *   ranks are P virtual shards in this GPU's memory.  The all-to-all that
+ *   gives every rank the full sequence of its own head group becomes an
+ *   on-device permutation; RoPE is applied at absolute positions on the way.
+ *   Each head group then runs causal GQA attention (forward and backward);
+ *   the inverse permutation returns outputs and gradients to sequence
+ *   shards.  The result equals full-sequence attention.
+ *
+ * Layouts (all bf16 tensors row-major, element type __nv_bfloat16):
+ *   "seq"  : x_seq[t][h][d],            t in [0,S_pad), h in [0,H), d in [0,D)
+ *            shard r is rows [r*S_loc, (r+1)*S_loc)
+ *   "head" : x_head[g][t][j][d],        g in [0,P), j in [0,H/P)
+ *            x_head[g][t][j] holds global head h = g*(H/P) + j of row t;
+ *            it is the concatenation of the P all-to-all messages rank g
+ *            receives.
+ *   lse    : float  [P][Hq/P][S_pad]    natural-log softmax denominators
+ *   pos,doc: int32  [S_pad]             absolute position / document id
+ *                                       (doc = -1 on pad rows)
+ *   rope_cs: float  [rope_len][D/2][2]  (cos, sin) of pair i at position p;
+ *                                       pair i rotates elements (i, i+D/2)
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers unless the name ends in _host.  The
+ *     caller owns every buffer; no call allocates or frees device memory.
+ *   - Tensor buffers must be 16-byte aligned; D must be 64 or 128.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and return after enqueueing.  Arguments are validated
+ *     on the host before anything is launched; a call that returns an error
+ *     has launched nothing.
+ *   - Byte offsets are 64-bit throughout, so S_pad*H*D may exceed 2^31.
+ *   - Device-side waits are bounded.  A kernel that gives up records it in
+ *     a device status word and exits; usp_device_status() reports it.
+ *   - Calls keep no state between invocations and may be issued from any
+ *     host thread.
+ */
+#ifndef USP_H_
+#define USP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define USP_ABI_VERSION 1
+
+typedef enum {
+  USP_OK = 0,
+  USP_ERR_INVALID_ARG = 1,          /* NULL/misaligned pointer, bad size, bad table */
+  USP_ERR_HEADS_NOT_DIVISIBLE = 2,  /* P does not divide Hq or Hkv, or Hkv does not divide Hq */
+  USP_ERR_UNSUPPORTED = 3,          /* e.g. D not in {64,128}, causal != 1 */
+  USP_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
+  USP_ERR_TIMEOUT = 5               /* a device-side wait gave up (see usp_device_status) */
+} usp_status;
+
+/* Problem description shared by all calls. */
+typedef struct {
+  int64_t S;                        /* valid tokens (sum of document lengths), >= 0 */
+  int32_t P;                        /* Ulysses degree = number of virtual shards, >= 1 */
+  int32_t Hq, Hkv, D;               /* query heads, key/value heads, head dim (64|128) */
+  const int32_t* cu_seqlens;        /* device int32 [n_docs+1], global document
+                                       boundaries; NULL => one document [0,S) */
+  const int32_t* cu_seqlens_host;   /* optional host copy of cu_seqlens; when given
+                                       it is checked (cu[0]=0, non-decreasing,
+                                       cu[n_docs]=S) before launch */
+  int32_t n_docs;                   /* documents in cu_seqlens (ignored if NULL) */
+  int32_t causal;                   /* must be 1 (causal within each document) */
+  float scale;                      /* softmax scale; 0 => 1/sqrt(D) */
+} usp_dims;
+
+/*
+ * usp_pad_shard -- shard + pad one activation tensor and (optionally) emit
+ * the absolute positions and document ids of the padded rows.
+ * (SpecForge #728, Modifications: inputs and absolute positions are sharded
+ * and padded across the SP group; verl #45: sequence lengths padded for SP
+ * alignment; Megatron-LM #7, Purpose: positions from the GLOBAL cu_seqlens.)
+ *
+ *   x     [S][H][D] bf16 (input, unpadded)
+ *   x_seq [S_pad][H][D] bf16 (output): rows < S copied, rows >= S zero.
+ *         x_seq == x is allowed (in place; the buffer must hold S_pad rows).
+ *   pos   [S_pad] int32 or NULL: t - cu[doc(t)]; pad rows keep counting in
+ *         the last document.
+ *   doc   [S_pad] int32 or NULL: document index of row t, -1 for pad rows.
+ * x may be NULL with H = 0 to emit only pos/doc.
+ */
+usp_status usp_pad_shard(const usp_dims* dims, const void* x, int32_t H,
+                         void* x_seq, int32_t* pos, int32_t* doc, void* stream);
+
+/*
+ * usp_seq_to_head_rope -- the seq->head all-to-all (SpecForge #728,
+ * Modifications: separate Q/K/V all-to-alls before local attention), fused
+ * with RoPE at absolute positions.
+ *
+ *   x_seq  [S_pad][H][D] bf16 -> x_head [P][S_pad][H/P][D] bf16
+ *   rope_mode 0: plain permutation (V, dO); pos/rope_cs may be NULL.
+ *   rope_mode 1: rotate every (d, d+D/2) pair of row t by the table entry
+ *                at pos[t]; -1 rotates by the negated angle.
+ *   Rounding (identical in every kernel): with x1 = x[d], x2 = x[d+D/2],
+ *   (c, s) = rope_cs[pos][d] and s negated for mode -1, in IEEE fp32 with
+ *   no fused multiply-add:  y[d] = bf16_rne(x1*c - x2*s),
+ *                           y[d+D/2] = bf16_rne(x2*c + x1*s).
+ *   rope_len must be >= S_pad (or > the largest position when
+ *   cu_seqlens_host is given): USP_ERR_INVALID_ARG otherwise
+ *   (Megatron-LM #7, Purpose: the table must cover the padded length).
+ */
+usp_status usp_seq_to_head_rope(const usp_dims* dims, const void* x_seq, int32_t H,
+                                const int32_t* pos, const float* rope_cs,
+                                int64_t rope_len, int32_t rope_mode,
+                                void* x_head, void* stream);
+
+/*
+ * usp_attn_fwd -- local causal GQA attention of every head group
+ * (SpecForge #728, Modifications: local attention after the all-to-all;
+ * Accuracy Test: equal to full-sequence attention).
+ *
+ * For group g, local query head j (global h = g*Hq/P + j, reading KV head
+ * h / (Hq/Hkv)) and row t with doc(t) >= 0:
+ *   O[t]   = sum_{u in M(t)} softmax_u(scale * q_t . k_u) v_u
+ *   LSE[t] = ln sum_{u in M(t)} exp(scale * q_t . k_u)
+ *   M(t)   = { u : doc(u) == doc(t), u <= t }.
+ * Rows with doc(t) = -1 (padding) get O = 0 and LSE = -inf.
+ *   q_h [P][S_pad][Hq/P][D], k_h/v_h [P][S_pad][Hkv/P][D] (bf16, head layout)
+ *   doc [S_pad] int32 (from usp_pad_shard)
+ *   o_h [P][S_pad][Hq/P][D] bf16 (output), lse [P][Hq/P][S_pad] fp32 (output)
+ * fp32 accumulation; no atomics, so the result is deterministic.
+ */
+usp_status usp_attn_fwd(const usp_dims* dims, const void* q_h, const void* k_h,
+                        const void* v_h, const int32_t* doc, void* o_h, float* lse,
+                        void* stream);
+
+/*
+ * usp_attn_bwd -- gradients of loss L with dL/dO = dO through usp_attn_fwd
+ * (SpecForge #728, Accuracy Test: gradient parity with full-sequence
+ * attention; verl #45: SP and non-SP fwd+bwd agree).
+ *   P_tu = exp(scale q_t.k_u - LSE_t),   delta_t = sum_d dO_t[d] O_t[d]
+ *   dV_u = sum_t P_tu dO_t,   dS_tu = P_tu (dO_t.v_u - delta_t)
+ *   dQ_t = scale sum_u dS_tu k_u,   dK_u = scale sum_t dS_tu q_t
+ * dK/dV of a KV head are summed over the Hq/Hkv query heads reading it.
+ * Gradients of pad rows are 0.
+ *   inputs as usp_attn_fwd plus o_h, lse (its outputs) and do_h
+ *   (upstream gradient, head layout); outputs dq_h, dk_h, dv_h (bf16,
+ *   head layout, same shapes as q_h, k_h, v_h).
+ *   workspace: device scratch of at least usp_attn_bwd_workspace(dims)
+ *   bytes, 256-byte aligned, not used concurrently by another call.
+ */
+usp_status usp_attn_bwd(const usp_dims* dims, const void* q_h, const void* k_h,
+                        const void* v_h, const void* o_h, const float* lse,
+                        const void* do_h, const int32_t* doc, void* dq_h, void* dk_h,
+                        void* dv_h, void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace usp_attn_bwd needs for dims (fp32 dQ accumulator and
+ * per-row delta).  Returns 0 for invalid dims. */
+size_t usp_attn_bwd_workspace(const usp_dims* dims);
+
+/*
+ * usp_head_to_seq -- the inverse all-to-all (head -> seq), used for O and
+ * for the gradients; rope_mode -1 applies the inverse rotation so that dQ
+ * and dK become gradients of the pre-RoPE inputs.  Same rounding and table
+ * rules as usp_seq_to_head_rope.
+ *   x_head [P][S_pad][H/P][D] bf16 -> x_seq [S_pad][H][D] bf16
+ */
+usp_status usp_head_to_seq(const usp_dims* dims, const void* x_head, int32_t H,
+                           const int32_t* pos, const float* rope_cs, int64_t rope_len,
+                           int32_t rope_mode, void* x_seq, void* stream);
+
+/*
+ * usp_rope_table -- fill a HOST buffer out_host[n_pos][D/2][2] with
+ * fp32(cos(theta)*m), fp32(sin(theta)*m) where theta = p * inv_freq_i is
+ * evaluated in double, inv_freq_i = base^(-2i/D), and for yarn_factor > 1
+ * the YaRN blend (Peng et al. 2023): pairs turning more than 32 times over
+ * yarn_orig_ctx keep inv_freq_i, pairs turning less than once use
+ * inv_freq_i / yarn_factor, a linear ramp over i in between, and
+ * m = 0.1 ln(yarn_factor) + 1 (m = 1 without YaRN).
+ * (SpecForge #728, Accuracy Test: Qwen3-8B with "YaRN context 131,072".)
+ */
+usp_status usp_rope_table(int64_t n_pos, int32_t D, double base, double yarn_factor,
+                          int32_t yarn_orig_ctx, float* out_host);
+
+/*
+ * usp_device_status -- synchronise `stream`, then report and clear the
+ * device status word: USP_ERR_TIMEOUT if a kernel's bounded wait gave up,
+ * USP_ERR_INVALID_ARG if a kernel met a position outside the RoPE table,
+ * USP_ERR_CUDA if the stream reported an error, else USP_OK.
+ */
+usp_status usp_device_status(void* stream);
+
+const char* usp_status_string(usp_status s);
+int usp_abi_version(void);
+
+/* Number of kernels this library has launched in this process so far
+ * (all devices, all streams); a diagnostic for benchmarks. */
+uint64_t usp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* USP_H_ */

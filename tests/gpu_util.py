@@ -1,0 +1,112 @@
+"""Helpers shared by the GPU parity tests: host<->device transfer of bf16
+bit patterns, and oracle evaluations restricted to sampled rows so that the
+full-size workloads can be checked in seconds."""
+import math
+
+import numpy as np
+import torch
+
+from oracle import usp_oracle as O
+
+# Tolerances (the same everywhere):
+O_MAX, O_MEAN = 2e-2, 2e-3          # attention output vs fp64
+GRAD_REL = 5e-2                     # dQ/dK/dV max|diff| / max|ref| per tensor
+LSE_ABS = 1e-3
+
+
+def to_dev(bits: np.ndarray) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.cuda().view(torch.bfloat16)
+
+
+def to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def check_o(got, ref, what="O"):
+    d = np.abs(got - ref)
+    assert d.max() <= O_MAX and d.mean() <= O_MEAN, (what, d.max(), d.mean())
+
+
+def check_grad(got, ref, what):
+    scale = max(np.abs(ref).max(), 1e-30)
+    err = np.abs(got - ref).max() / scale
+    assert err <= GRAD_REL, (what, err)
+    return err
+
+
+def check_lse(got, ref):
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    assert np.all(got[~fin] == ref[~fin])
+    if fin.any():
+        assert np.abs(got[fin] - ref[fin]).max() <= LSE_ABS
+
+
+class SampledOracle:
+    """Oracle values at chosen rows of one full-size problem.
+
+    Inputs are the pre-RoPE bf16 bits of the unpadded sequence; RoPE is the
+    exact fp64 rotation of the oracle (this is the end-to-end reference).
+    """
+
+    def __init__(self, q, k, v, do, cu, wl):
+        self.wl = wl
+        S, D = wl.S, wl.D
+        self.S = S
+        self.G = wl.Hq // wl.Hkv
+        self.scale = 1.0 / math.sqrt(D)
+        self.pos, self.doc = O.positions_docs(S, 1, cu)
+        self.cos, self.sin = O.rope_cos_sin(max(wl.table_len, S), D, wl.rope_base,
+                                            wl.yarn_factor, wl.yarn_orig_ctx)
+        self.q, self.k, self.v, self.do = q, k, v, do
+        self._kr = {}
+
+    def _rot(self, bits_rows, rows):
+        x = O.bf16_to_f64(bits_rows)
+        return O.rope_rotate(x[:, None, :], self.pos[rows], self.cos, self.sin)[:, 0]
+
+    def k_rot(self, kh):
+        if kh not in self._kr:
+            self._kr[kh] = self._rot(self.k[:, kh], np.arange(self.S))
+        return self._kr[kh]
+
+    def fwd_rows(self, h, rows):
+        kh = h // self.G
+        qr = np.zeros((self.S, self.wl.D))
+        qr[rows] = self._rot(self.q[rows, h], rows)
+        return O.attention_rows(qr, self.k_rot(kh), O.bf16_to_f64(self.v[:, kh]), self.doc,
+                                np.asarray(rows), self.scale)
+
+    def dq_rows(self, h, rows):
+        """Pre-RoPE dQ of head h at the given rows."""
+        kh = h // self.G
+        qr = np.zeros((self.S, self.wl.D))
+        qr[rows] = self._rot(self.q[rows, h], rows)
+        dq, _, _ = O.attention_bwd_head(qr, self.k_rot(kh), O.bf16_to_f64(self.v[:, kh]),
+                                        O.bf16_to_f64(self.do[:, h]), self.doc, self.scale,
+                                        rows=np.asarray(rows))
+        return O.rope_rotate(dq[:, None, :], self.pos[rows], self.cos, self.sin,
+                             inverse=True)[:, 0]
+
+    def dkv_tail(self, kh, u_lo, u_hi):
+        """Pre-RoPE dK and dV of KV head kh at keys [u_lo, u_hi), which must lie
+        in one document that ends at u_hi (so only queries >= u_lo see them)."""
+        rows = np.arange(u_lo, u_hi)
+        dk = np.zeros((u_hi - u_lo, self.wl.D))
+        dv = np.zeros_like(dk)
+        for i in range(self.G):
+            h = kh * self.G + i
+            qr = np.zeros((self.S, self.wl.D))
+            qr[rows] = self._rot(self.q[rows, h], rows)
+            _, a, b = O.attention_bwd_head(qr, self.k_rot(kh), O.bf16_to_f64(self.v[:, kh]),
+                                           O.bf16_to_f64(self.do[:, h]), self.doc, self.scale,
+                                           rows=rows)
+            dk += a[u_lo:u_hi]
+            dv += b[u_lo:u_hi]
+        dk = O.rope_rotate(dk[:, None, :], self.pos[rows], self.cos, self.sin, inverse=True)[:, 0]
+        return dk, dv

@@ -1,0 +1,195 @@
+"""GPU parity of the attention kernels and the whole USP pipeline against
+the fp64 oracle.
+
+* kernel parity: the oracle rotates Q/K with the bf16 recipe and permutes
+  them itself; those bits go to usp_attn_fwd/usp_attn_bwd, and the results
+  are compared with fp64 attention of the same bf16 values;
+* end-to-end parity: UlyssesAttention (pad -> all-to-all+RoPE -> attention
+  -> all-to-all back, forward and backward) against the oracle's
+  full-sequence fp64 computation with exact RoPE (the criterion of loss and
+  gradient parity with full-sequence attention);
+* full-size workloads, in the launch configuration the benchmark times,
+  checked on sampled rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import usp_oracle as O
+from ulysses_sequence_attention_usp_gb300 import binding as B
+from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, custom_workload, make_inputs
+from ulysses_sequence_attention_usp_gb300.pipeline import UlyssesAttention
+
+from gpu_util import (SampledOracle, check_grad, check_lse, check_o, to_bits, to_dev, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [  # S, P, Hq, Hkv, D, doc lengths (None = one sequence)
+    (256, 2, 4, 2, 64, None),             # the tiny workload
+    (1000, 2, 8, 2, 128, None),           # several tiles, ragged tail
+    (777, 4, 8, 4, 64, [100, 1, 300, 376]),  # packed documents, a doc of length 1
+    (130, 2, 2, 2, 128, [1, 129]),        # MHA (G = 1)
+    (30, 4, 8, 4, 128, None),             # padded 30 -> 32
+    (1, 8, 8, 8, 128, None),              # one token, fewer rows than ranks
+    (600, 2, 16, 2, 128, [200, 400]),     # G = 8 as in the packed 64/8 workload
+]
+
+
+def _setup(case, seed=0):
+    S, P, Hq, Hkv, D, lens = case
+    wl = custom_workload(S, P, Hq, Hkv, D, base=1.0e4, thd_lens=lens)
+    inp = make_inputs(wl, seed, lens=lens)
+    return wl, inp
+
+
+def _kernel_inputs(wl, inp):
+    """Oracle-made head-layout bf16 inputs (RoPE by the bf16 recipe)."""
+    P = wl.P
+    table = O.rope_table_f32(wl.S_pad, wl.D, wl.rope_base)
+    pos, doc = O.positions_docs(wl.S, P, inp.cu)
+    qh = O.seq_to_head(O.rope_recipe_bf16(O.shard_pad(inp.q, P), pos, table), P)
+    kh = O.seq_to_head(O.rope_recipe_bf16(O.shard_pad(inp.k, P), pos, table), P)
+    vh = O.seq_to_head(O.shard_pad(inp.v, P), P)
+    doh = O.seq_to_head(O.shard_pad(inp.do, P), P)
+    return qh, kh, vh, doh, doc
+
+
+def _dims(wl, cu):
+    cu_dev = None if cu is None else torch.from_numpy(cu.astype(np.int32)).cuda()
+    return B.make_dims(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_dev, cu)
+
+
+@pytest.mark.parametrize("case", SMALL)
+def test_attention_kernels_vs_fp64(case):
+    wl, inp = _setup(case)
+    qh, kh, vh, doh, doc = _kernel_inputs(wl, inp)
+    d = _dims(wl, inp.cu)
+    P, Sp, hq, hkv, D = wl.P, wl.S_pad, wl.Hq // wl.P, wl.Hkv // wl.P, wl.D
+    tq, tk, tv, tdo = to_dev(qh), to_dev(kh), to_dev(vh), to_dev(doh)
+    tdoc = torch.from_numpy(doc.astype(np.int32)).cuda()
+    o = torch.full((P, Sp, hq, D), 9.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((P, hq, Sp), 9.0, dtype=torch.float32, device="cuda")
+    B.usp_attn_fwd(d, tq, tk, tv, tdoc, o, lse)
+    ws_n = B.usp_attn_bwd_workspace(d)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+    dq = torch.full_like(tq, 9.0)
+    dk = torch.full_like(tk, 9.0)
+    dv = torch.full_like(tv, 9.0)
+    B.usp_attn_bwd(d, tq, tk, tv, o, lse, tdo, tdoc, dq, dk, dv, ws, ws_n)
+    B.usp_device_status()
+    scale = 1.0 / math.sqrt(D)
+    for g in range(P):
+        qf, kf, vf, dof = (O.bf16_to_f64(x[g]) for x in (qh, kh, vh, doh))
+        o_ref, lse_ref = O.attention_fwd(qf, kf, vf, doc, scale)
+        check_o(to_f64(o[g]), o_ref)
+        check_lse(lse[g].cpu().numpy().astype(np.float64), lse_ref)
+        dq_ref, dk_ref, dv_ref = O.attention_bwd(qf, kf, vf, dof, doc, scale)
+        check_grad(to_f64(dq[g]), dq_ref, "dq")
+        check_grad(to_f64(dk[g]), dk_ref, "dk")
+        check_grad(to_f64(dv[g]), dv_ref, "dv")
+        pad = doc < 0
+        assert not to_f64(o[g])[pad].any() and not to_f64(dq[g])[pad].any()
+        assert not to_f64(dk[g])[pad].any() and not to_f64(dv[g])[pad].any()
+
+
+@pytest.mark.parametrize("case", SMALL)
+def test_pipeline_vs_full_sequence(case):
+    wl, inp = _setup(case, seed=1)
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                          rope_base=wl.rope_base)
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    dq, dk, dv = ua.step(q, k, v, do)
+    ua.check()
+    cos, sin = O.rope_cos_sin(wl.S_pad, wl.D, wl.rope_base)
+    f = lambda b: O.bf16_to_f64(b)  # noqa: E731
+    ref = O.full_sequence(f(inp.q), f(inp.k), f(inp.v), f(inp.do), inp.cu, cos, sin,
+                          1.0 / math.sqrt(wl.D))
+    S = wl.S
+    check_o(to_f64(ua.o)[:S], ref["o"])
+    lse = ua.lse.cpu().numpy().astype(np.float64).reshape(wl.Hq, wl.S_pad)[:, :S]
+    check_lse(lse, ref["lse"])
+    check_grad(to_f64(dq)[:S], ref["dq"], "dq")
+    check_grad(to_f64(dk)[:S], ref["dk"], "dk")
+    check_grad(to_f64(dv)[:S], ref["dv"], "dv")
+    loss = float(ua.loss(do))
+    assert abs(loss - ref["loss"]) <= 1e-2 * float(np.abs(ref["o"] * f(inp.do)).sum())
+    # outputs past S (padding) are zero
+    assert not to_f64(ua.o)[S:].any() and not to_f64(dq)[S:].any()
+
+
+def test_attention_is_deterministic():
+    wl, inp = _setup((1000, 2, 8, 2, 128, None), seed=2)
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, rope_base=wl.rope_base)
+    q, k, v = (to_dev(x) for x in (inp.q, inp.k, inp.v))
+    a = ua.forward(q, k, v).clone()
+    la = ua.lse.clone()
+    b = ua.forward(q, k, v)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(la, ua.lse)
+
+
+# --------------------------------------------------------------- full sizes
+
+def _full_case(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, 0)
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                          rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
+                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len)
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    ua.step(q, k, v, do)
+    ua.check()
+    return wl, inp, ua
+
+
+@pytest.mark.parametrize("name", ["sp8_120k", "thd64k", "long32k_pad", "qwen8k"])
+def test_full_workload_sampled(name):
+    wl, inp, ua = _full_case(name)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
+    rng = np.random.default_rng(5)
+    S = wl.S
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, S // 2, S - 1], rng.integers(0, S, 10)]))
+    o = ua.o[:S]
+    lse = ua.lse.reshape(wl.Hq, wl.S_pad)
+    dq = ua.dq[:S]
+    heads = sorted({0, wl.Hq - 1, int(rng.integers(0, wl.Hq))})
+    got_o, ref_o, got_l, ref_l, got_dq, ref_dq = [], [], [], [], [], []
+    for h in heads:
+        r_o, r_l = orc.fwd_rows(h, rows)
+        got_o.append(to_f64(o[rows, h]))
+        ref_o.append(r_o)
+        got_l.append(lse[h, rows].cpu().numpy().astype(np.float64))
+        ref_l.append(r_l)
+        got_dq.append(to_f64(dq[rows, h]))
+        ref_dq.append(orc.dq_rows(h, rows))
+    check_o(np.concatenate(got_o), np.concatenate(ref_o))
+    check_lse(np.concatenate(got_l), np.concatenate(ref_l))
+    check_grad(np.concatenate(got_dq), np.concatenate(ref_dq), "dq")
+    # dK/dV at the last rows of a document: only queries at or after them
+    # see those keys, so the oracle needs just those query rows
+    ends = [S] if inp.cu is None else [int(inp.cu[-1]), int(inp.cu[3])]
+    for end in ends:
+        lo = end - 48
+        for kh in sorted({0, wl.Hkv - 1}):
+            r_dk, r_dv = orc.dkv_tail(kh, lo, end)
+            check_grad(to_f64(ua.dk[lo:end, kh]), r_dk, "dk")
+            check_grad(to_f64(ua.dv[lo:end, kh]), r_dv, "dv")
+
+
+def test_padded_matches_unpadded_long():
+    # S = 32766 pads to 32768 over P = 8; over P = 2 it needs no padding.
+    wl8 = WORKLOADS["long32k_pad"]
+    inp = make_inputs(wl8, 0, with_do=True)
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    outs = []
+    for P in (8, 2):
+        ua = UlyssesAttention(wl8.S, P, wl8.Hq, wl8.Hkv, wl8.D, rope_base=wl8.rope_base,
+                              rope_len=32768)
+        dq, dk, dv = ua.step(q, k, v, do)
+        ua.check()
+        outs.append([t[:wl8.S].clone() for t in (ua.o, dq, dk, dv)])
+    for a, b in zip(*outs):
+        fa, fb = a.float(), b.float()
+        assert (fa - fb).abs().max().item() <= 2e-2 * max(1.0, fb.abs().max().item())

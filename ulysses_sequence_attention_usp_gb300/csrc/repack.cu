@@ -1,0 +1,207 @@
+// Shard/pad and the Ulysses all-to-all as on-device permutations.
+//
+// SpecForge PR #728 "feat(dspark): add Ulysses sequence parallel training",
+// Modifications: sequences and their absolute positions are padded and
+// sharded across the SP group, and Q, K, V each go through an all-to-all
+// before local attention.  On one GPU the P ranks are P slices of the same
+// buffer, so the all-to-all is the permutation
+//     x_head[g][t][j][:] = x_seq[t][g*H/P + j][:]
+// in which every (t, g) pair moves one contiguous chunk of H/P*D elements.
+// RoPE at the absolute position pos[t] (Megatron-LM PR #7 "GLM-5.2 131k
+// context parallelism", Purpose: positions from the global cu_seqlens) is
+// fused into the permutation, so each element is read once and written once.
+//
+// Both kernels are HBM-bound: 16-byte loads and stores, streaming cache
+// hints, one warp per token row and several heads in flight per thread.
+#include "usp_common.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// ---------------------------------------------------------------- pad/shard
+// Largest d in [0, n_docs) with cu[d] <= t (documents are contiguous).
+__device__ __forceinline__ int doc_of(const int32_t* cu, int n_docs, int64_t t) {
+  int lo = 0, hi = n_docs - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(256) pad_shard_kernel(
+    const uint4* __restrict__ x, uint4* __restrict__ y, int64_t n_valid_vec,
+    int64_t n_total_vec, int inplace, int32_t* __restrict__ pos, int32_t* __restrict__ doc,
+    const int32_t* __restrict__ cu, int n_docs, int64_t S, int64_t S_pad) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  for (int64_t i = i0; i < n_total_vec; i += stride) {
+    if (i < n_valid_vec) {
+      if (!inplace) st_stream(y + i, ld_stream(x + i));
+    } else {
+      st_stream(y + i, zero);
+    }
+  }
+  if (pos == nullptr && doc == nullptr) return;
+  for (int64_t t = i0; t < S_pad; t += stride) {
+    int d = 0;
+    int64_t start = 0;
+    if (cu != nullptr) {
+      d = doc_of(cu, n_docs, t);
+      start = __ldg(cu + d);
+    }
+    if (pos) pos[t] = (int32_t)(t - start);
+    if (doc) doc[t] = t < S ? d : -1;
+  }
+}
+
+// ------------------------------------------------------------------ repack
+// One warp per token row t.  A head's D elements are covered by D/16
+// threads; thread `sub` owns pairs [8*sub, 8*sub+8): elements d = 8*sub..+7
+// and their rotation partners d + D/2.  32/(D/16) heads are processed per
+// step and kUnroll steps are loaded before any is stored.
+template <int D, int MODE, bool TO_HEAD>
+__global__ void __launch_bounds__(256) repack_kernel(
+    const bf16* __restrict__ src, bf16* __restrict__ dst, const int32_t* __restrict__ pos,
+    const float* __restrict__ cs, int64_t rope_len, int64_t S_pad, int H, int hp,
+    unsigned* status) {
+  constexpr int TPH = D / 16;
+  constexpr int HPI = 32 / TPH;
+  constexpr int kUnroll = 4;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % TPH;
+  const int slot = lane / TPH;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+
+  for (int64_t t = warp; t < S_pad; t += nwarps) {
+    float c[8], s[8];
+    bool zero_row = false;
+    if (MODE != 0) {
+      const int p = __ldg(pos + t);
+      if (p < 0 || (int64_t)p >= rope_len) {
+        if (lane == 0) usp::set_status(status, usp::kErrRopeRange);
+        zero_row = true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { c[i] = 0.f; s[i] = 0.f; }
+      } else {
+        const float4* tp = reinterpret_cast<const float4*>(cs + ((int64_t)p * (D / 2) + 8 * sub) * 2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 v = __ldg(tp + i);
+          c[2 * i] = v.x; s[2 * i] = v.y; c[2 * i + 1] = v.z; s[2 * i + 1] = v.w;
+        }
+        if (MODE < 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) s[i] = -s[i];
+        }
+      }
+    }
+    for (int h0 = slot; h0 < H; h0 += kUnroll * HPI) {
+      uint4 lo[kUnroll], hi[kUnroll];
+      int64_t doff[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int h = h0 + u * HPI;
+        doff[u] = -1;
+        if (h < H) {
+          const int g = h / hp, j = h - g * hp;
+          const int64_t seq_off = (t * H + h) * (int64_t)D;
+          const int64_t head_off = (((int64_t)g * S_pad + t) * hp + j) * (int64_t)D;
+          const bf16* sp = src + (TO_HEAD ? seq_off : head_off);
+          doff[u] = TO_HEAD ? head_off : seq_off;
+          lo[u] = ld_stream(sp + 8 * sub);
+          hi[u] = ld_stream(sp + D / 2 + 8 * sub);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        if (doff[u] < 0) continue;
+        uint4 a = lo[u], b = hi[u];
+        if (MODE != 0) {
+          const bf16* xa = reinterpret_cast<const bf16*>(&lo[u]);
+          const bf16* xb = reinterpret_cast<const bf16*>(&hi[u]);
+          bf16* ya = reinterpret_cast<bf16*>(&a);
+          bf16* yb = reinterpret_cast<bf16*>(&b);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float x1 = __bfloat162float(xa[i]);
+            const float x2 = __bfloat162float(xb[i]);
+            // IEEE fp32, each product rounded separately (no FMA contraction)
+            const float y1 = __fsub_rn(__fmul_rn(x1, c[i]), __fmul_rn(x2, s[i]));
+            const float y2 = __fadd_rn(__fmul_rn(x2, c[i]), __fmul_rn(x1, s[i]));
+            ya[i] = __float2bfloat16_rn(y1);
+            yb[i] = __float2bfloat16_rn(y2);
+          }
+          if (zero_row) { a = make_uint4(0, 0, 0, 0); b = a; }
+        }
+        bf16* dp = dst + doff[u];
+        st_stream(dp + 8 * sub, a);
+        st_stream(dp + D / 2 + 8 * sub, b);
+      }
+    }
+  }
+}
+
+int repack_grid(int64_t S_pad) {
+  int64_t blocks = (S_pad + 7) / 8;  // 8 warps (tokens) per block
+  const int64_t cap = 152 * 64;      // grid-stride beyond this
+  if (blocks > cap) blocks = cap;
+  return (int)(blocks < 1 ? 1 : blocks);
+}
+
+template <int D, bool TO_HEAD>
+cudaError_t launch_mode(int mode, const bf16* src, bf16* dst, const int32_t* pos,
+                        const float* cs, int64_t rope_len, int64_t S_pad, int H, int hp,
+                        unsigned* status, cudaStream_t st) {
+  const int grid = repack_grid(S_pad);
+  if (mode == 0)
+    repack_kernel<D, 0, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp, status);
+  else if (mode > 0)
+    repack_kernel<D, 1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp, status);
+  else
+    repack_kernel<D, -1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp, status);
+  usp_count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t usp_launch_pad_shard(const usp::Geometry& g, const void* x, int H, void* x_seq,
+                                 int32_t* pos, int32_t* doc, const int32_t* cu, int n_docs,
+                                 cudaStream_t st) {
+  const int64_t row_vec = (int64_t)H * g.D * 2 / 16;
+  const int64_t n_valid = (x_seq != nullptr) ? g.S * row_vec : 0;
+  const int64_t n_total = (x_seq != nullptr) ? g.S_pad * row_vec : 0;
+  int64_t work = n_total > g.S_pad ? n_total : g.S_pad;
+  int64_t blocks = (work + 255) / 256;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  if (blocks < 1) blocks = 1;
+  pad_shard_kernel<<<(int)blocks, 256, 0, st>>>(
+      reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_seq), n_valid, n_total,
+      x == x_seq ? 1 : 0, pos, doc, cu, n_docs, g.S, g.S_pad);
+  usp_count_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t usp_launch_repack(const usp::Geometry& g, const void* src, int H, const int32_t* pos,
+                              const float* rope_cs, int64_t rope_len, int rope_mode,
+                              bool to_head, void* dst, cudaStream_t st) {
+  const int hp = H / g.P;
+  const bf16* s = reinterpret_cast<const bf16*>(src);
+  bf16* d = reinterpret_cast<bf16*>(dst);
+  if (g.D == 128)
+    return to_head ? launch_mode<128, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st)
+                   : launch_mode<128, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st);
+  return to_head ? launch_mode<64, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st)
+                 : launch_mode<64, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st);
+}

@@ -1,0 +1,50 @@
+// Shared device helpers of the USP library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "usp.h"
+
+namespace usp {
+
+// Device status word: bit 0 = a bounded wait gave up, bit 1 = a position
+// fell outside the RoPE table.  Kernels receive its address as an argument;
+// usp_device_status reports and clears it.
+enum : unsigned { kErrTimeout = 1u, kErrRopeRange = 2u };
+
+__device__ __forceinline__ void set_status(unsigned* word, unsigned bits) {
+  if (word) atomicOr(word, bits);
+}
+
+// Host side helpers (usp_api.cu).
+struct Geometry {
+  int64_t S, S_pad, S_loc;
+  int P, Hq, Hkv, D, hq, hkv, G;
+  float scale;
+  unsigned* status;   // device address of the status word of the current device
+};
+
+}  // namespace usp
+
+// Host-side count of kernel launches (usp_launch_count); every launcher
+// adds the kernels it enqueued.
+void usp_count_launches(unsigned n);
+
+// Kernel launchers implemented per translation unit; all return cudaError_t
+// of the launch (cudaGetLastError after the launch).
+cudaError_t usp_launch_pad_shard(const usp::Geometry& g, const void* x, int H, void* x_seq,
+                                 int32_t* pos, int32_t* doc, const int32_t* cu, int n_docs,
+                                 cudaStream_t st);
+cudaError_t usp_launch_repack(const usp::Geometry& g, const void* src, int H, const int32_t* pos,
+                              const float* rope_cs, int64_t rope_len, int rope_mode,
+                              bool to_head, void* dst, cudaStream_t st);
+cudaError_t usp_launch_attn_fwd(const usp::Geometry& g, const void* q, const void* k,
+                                const void* v, const int32_t* doc, const int32_t* cu,
+                                void* o, float* lse, cudaStream_t st);
+cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const void* k,
+                                const void* v, const void* o, const float* lse,
+                                const void* dout, const int32_t* doc, const int32_t* cu,
+                                void* dq, void* dk, void* dv, void* ws, cudaStream_t st);
+size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g);

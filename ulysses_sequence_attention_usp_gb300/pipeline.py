@@ -1,0 +1,97 @@
+"""The USP attention forward + backward as one object over the C ABI.
+
+:class:`UlyssesAttention` owns the device buffers of one problem size and
+runs the hot path by calling the library's entry points in order
+(SpecForge PR #728 "feat(dspark): add Ulysses sequence parallel training",
+Modifications):
+
+forward:   pad/shard Q,K,V  ->  seq->head all-to-all (+RoPE on Q,K)
+           ->  local causal GQA attention per head group  ->  head->seq (O)
+backward:  pad/shard dO  ->  seq->head (dO)  ->  attention backward
+           ->  head->seq (dQ, dK with the inverse rotation; dV)
+
+PyTorch provides device memory and the stream only; every step runs in the
+library's kernels.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+class UlyssesAttention:
+    def __init__(self, S, P, Hq, Hkv, D, cu_seqlens=None, rope_base=1.0e4, yarn_factor=1.0,
+                 yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None):
+        self.S, self.P, self.Hq, self.Hkv, self.D = int(S), int(P), int(Hq), int(Hkv), int(D)
+        self.S_pad = -(-self.S // self.P) * self.P
+        self.device = torch.device(device)
+        dev = self.device
+        self.cu_host = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, np.int32)
+        self.cu_dev = None if self.cu_host is None else torch.from_numpy(self.cu_host).to(dev)
+        self.dims = B.make_dims(S, P, Hq, Hkv, D, self.cu_dev, self.cu_host, scale)
+        self.rope_len = int(rope_len) if rope_len else self.S_pad
+        if rope_table is None:
+            rope_table = B.usp_rope_table(self.rope_len, D, rope_base, yarn_factor, yarn_orig_ctx)
+        self.rope_host = rope_table
+        self.rope = torch.from_numpy(np.ascontiguousarray(rope_table)).to(dev)
+        Sp, hq, hkv = self.S_pad, Hq // P, Hkv // P
+        bf = torch.bfloat16
+        e = lambda *s, dt=bf: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        self.pos = e(Sp, dt=torch.int32)
+        self.doc = e(Sp, dt=torch.int32)
+        self.q_seq, self.k_seq, self.v_seq = e(Sp, Hq, D), e(Sp, Hkv, D), e(Sp, Hkv, D)
+        self.do_seq = e(Sp, Hq, D)
+        self.q_h, self.k_h, self.v_h = e(P, Sp, hq, D), e(P, Sp, hkv, D), e(P, Sp, hkv, D)
+        self.do_h, self.o_h = e(P, Sp, hq, D), e(P, Sp, hq, D)
+        self.lse = e(P, hq, Sp, dt=torch.float32)
+        self.dq_h, self.dk_h, self.dv_h = e(P, Sp, hq, D), e(P, Sp, hkv, D), e(P, Sp, hkv, D)
+        self.o, self.dq = e(Sp, Hq, D), e(Sp, Hq, D)
+        self.dk, self.dv = e(Sp, Hkv, D), e(Sp, Hkv, D)
+        self.ws_bytes = B.usp_attn_bwd_workspace(self.dims)
+        self.ws = e(max(1, self.ws_bytes), dt=torch.uint8)
+
+    # -- steps -------------------------------------------------------------
+    def forward(self, q, k, v, stream=None):
+        """q [S][Hq][D], k/v [S][Hkv][D] bf16 device tensors (pre-RoPE).
+        Returns O [S_pad][Hq][D] (rows >= S are 0) in sequence layout."""
+        d, st = self.dims, stream
+        B.usp_pad_shard(d, q, self.Hq, self.q_seq, self.pos, self.doc, st)
+        B.usp_pad_shard(d, k, self.Hkv, self.k_seq, None, None, st)
+        B.usp_pad_shard(d, v, self.Hkv, self.v_seq, None, None, st)
+        B.usp_seq_to_head_rope(d, self.q_seq, self.Hq, self.pos, self.rope, self.rope_len, 1,
+                               self.q_h, st)
+        B.usp_seq_to_head_rope(d, self.k_seq, self.Hkv, self.pos, self.rope, self.rope_len, 1,
+                               self.k_h, st)
+        B.usp_seq_to_head_rope(d, self.v_seq, self.Hkv, None, None, 0, 0, self.v_h, st)
+        B.usp_attn_fwd(d, self.q_h, self.k_h, self.v_h, self.doc, self.o_h, self.lse, st)
+        B.usp_head_to_seq(d, self.o_h, self.Hq, None, None, 0, 0, self.o, st)
+        return self.o
+
+    def backward(self, do, stream=None):
+        """do [S][Hq][D] bf16 (dL/dO).  Returns dQ, dK, dV [S_pad][H][D]: the
+        gradients of the pre-RoPE sequence-sharded inputs."""
+        d, st = self.dims, stream
+        B.usp_pad_shard(d, do, self.Hq, self.do_seq, None, None, st)
+        B.usp_seq_to_head_rope(d, self.do_seq, self.Hq, None, None, 0, 0, self.do_h, st)
+        B.usp_attn_bwd(d, self.q_h, self.k_h, self.v_h, self.o_h, self.lse, self.do_h, self.doc,
+                       self.dq_h, self.dk_h, self.dv_h, self.ws, self.ws_bytes, st)
+        B.usp_head_to_seq(d, self.dq_h, self.Hq, self.pos, self.rope, self.rope_len, -1,
+                          self.dq, st)
+        B.usp_head_to_seq(d, self.dk_h, self.Hkv, self.pos, self.rope, self.rope_len, -1,
+                          self.dk, st)
+        B.usp_head_to_seq(d, self.dv_h, self.Hkv, None, None, 0, 0, self.dv, st)
+        return self.dq, self.dk, self.dv
+
+    def step(self, q, k, v, do, stream=None):
+        self.forward(q, k, v, stream)
+        return self.backward(do, stream)
+
+    def loss(self, do) -> torch.Tensor:
+        """sum(O * dO) over the valid rows, in fp32 on the device (reporting
+        only; not part of the hot path)."""
+        return (self.o[:self.S].float() * do.float()).sum()
+
+    def check(self, stream=None):
+        B.usp_device_status(stream)
