@@ -78,7 +78,8 @@ def _repack_case(S, P, Hq, Hkv, D, cu, which, mode, rows=None, base=1.0e4, f=1.0
     sub = x[rows]
     if mode != 0:
         sub = O.rope_recipe_bf16(sub, pos[rows], table, inverse=mode < 0)
-    want = O.seq_to_head(sub, P)            # the permutation acts row by row
+    # the permutation acts row by row: row t, head g*H/P + j -> [g][t][j]
+    want = sub.reshape(len(rows), P, H // P, D).transpose(1, 0, 2, 3)
     assert np.array_equal(got[:, rows], want)
 
 
