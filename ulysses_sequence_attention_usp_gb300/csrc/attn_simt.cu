@@ -349,7 +349,7 @@ Args make_args(const usp::Geometry& g) {
 
 }  // namespace
 
-cudaError_t usp_launch_attn_fwd(const usp::Geometry& g, const void* q, const void* k,
+cudaError_t usp_launch_attn_fwd_simt(const usp::Geometry& g, const void* q, const void* k,
                                 const void* v, const int32_t* doc, const int32_t* cu,
                                 void* o, float* lse, cudaStream_t st) {
   Args a = make_args(g);

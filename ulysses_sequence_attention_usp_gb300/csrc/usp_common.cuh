@@ -48,3 +48,9 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
                                 const void* dout, const int32_t* doc, const int32_t* cu,
                                 void* dq, void* dk, void* dv, void* ws, cudaStream_t st);
 size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g);
+
+// Tensor map (TMA descriptor) over a head-layout bf16 tensor [P][S_pad][heads][D],
+// boxes of 64 columns x box_rows rows with 128-byte swizzle (attn_fwd_tc.cu).
+struct CUtensorMap_st;
+bool usp_make_head_map(CUtensorMap_st* map, const void* base, int heads, int D, int64_t S_pad,
+                       int P, int box_rows);
