@@ -155,14 +155,17 @@ usp_status usp_attn_fwd(const usp_dims* dims, const void* q_h, const void* k_h,
  *   head layout, same shapes as q_h, k_h, v_h).
  *   workspace: device scratch of at least usp_attn_bwd_workspace(dims)
  *   bytes, 256-byte aligned, not used concurrently by another call.
+ * dQ is produced by a query-stationary pass and dK/dV by a key-stationary
+ * pass, so no atomics are used and the result is deterministic.
  */
 usp_status usp_attn_bwd(const usp_dims* dims, const void* q_h, const void* k_h,
                         const void* v_h, const void* o_h, const float* lse,
                         const void* do_h, const int32_t* doc, void* dq_h, void* dk_h,
                         void* dv_h, void* workspace, size_t ws_bytes, void* stream);
 
-/* Bytes of workspace usp_attn_bwd needs for dims (fp32 dQ accumulator and
- * per-row delta).  Returns 0 for invalid dims. */
+/* Bytes of workspace usp_attn_bwd needs for dims: two fp32 arrays of
+ * P*(Hq/P)*S_pad + 128 entries (delta_t and LSE_t*log2(e)), each rounded up
+ * to 256 bytes.  Returns 0 for invalid dims. */
 size_t usp_attn_bwd_workspace(const usp_dims* dims);
 
 /*

@@ -64,7 +64,7 @@ def test_causal_flag_and_scale_checked():
 def test_bwd_workspace_size_and_checks():
     d = _dims()
     ws = B.usp_attn_bwd_workspace(d)
-    assert ws >= 2 * 128 * 256 * 4                  # fp32 dQ accumulator
+    assert ws >= 2 * (2 * 2 * 256) * 4              # delta and LSE*log2e, fp32
     assert B.usp_attn_bwd_workspace(_dims(P=3)) == 0
     args = [ctypes.byref(d)] + [FAKE] * 11
     assert B.raw_call("usp_attn_bwd", *args, ctypes.c_size_t(ws - 1), None) == 1

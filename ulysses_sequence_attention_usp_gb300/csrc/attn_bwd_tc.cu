@@ -1,0 +1,605 @@
+// Causal per-document GQA attention backward on the tcgen05 tensor cores.
+//
+// Gradients of L with dL/dO = dO through the forward (SpecForge PR #728
+// "feat(dspark): add Ulysses sequence parallel training", Accuracy Test:
+// gradient parity with full-sequence attention):
+//   P_tu  = exp(scale q_t.k_u - LSE_t),     delta_t = dO_t . O_t
+//   dS_tu = P_tu (dO_t . v_u - delta_t)
+//   dV_u  = sum_t P_tu dO_t,   dK_u = scale sum_t dS_tu q_t,
+//   dQ_t  = scale sum_u dS_tu k_u.
+//
+// Three kernels, no atomics (so the result is deterministic):
+//   delta_kernel  delta_t = dO_t . O_t                         (HBM-bound)
+//   dkdv_kernel   one CTA per 128 key rows of one KV head; loops over the
+//                 Hq/Hkv query heads of the group and the query tiles that
+//                 see these keys, accumulating dV and dK in TMEM:
+//                   S^T  = K Q^T,  dP^T = V dO^T        (SS MMA)
+//                   P^T, dS^T computed per key row by 128 threads, written
+//                   as bf16 over S^T and dP^T in TMEM
+//                   dV  += P^T dO,  dK += dS^T Q        (TS MMA)
+//   dq_kernel     one CTA per 128 query rows of one query head; loops over
+//                 key tiles:  S = Q K^T, dP = dO V^T (SS), dS over S (bf16),
+//                 dQ += dS K (TS).
+// Both reuse the forward's warp roles: warp 0 TMA producer, warp 1 TMEM
+// owner and MMA issuer, warps 4-7 the per-row elementwise work and the
+// epilogue.  All waits are bounded (status word on timeout).
+#include "tc_ptx.cuh"
+#include "usp_common.cuh"
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+constexpr int BT = 128;                       // rows per tile (queries and keys)
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+  static constexpr int NB = D / 64;
+  static constexpr int BOX = 128 * 128;
+  static constexpr int TILE = NB * BOX;
+  static constexpr int NSTAGE = 4;            // ring slots (two per iteration)
+  static constexpr int FIX_OFF = 0;           // two stationary tiles
+  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr int BAR_OFF = RING_OFF + NSTAGE * TILE;
+  static constexpr int SMEM = BAR_OFF + 512 + 1024;
+};
+
+struct Bars {
+  uint64_t fix_full;
+  uint64_t ring_full[8];
+  uint64_t ring_empty[8];
+  uint64_t s_full;
+  uint64_t dp_full;
+  uint64_t p_full;
+  uint64_t mma_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Params {
+  const int32_t* doc;
+  const int32_t* cu;
+  const float* lse2;     // [P][hq][S_pad] LSE*log2(e); +inf for rows without keys
+  const float* delta;    // [P][hq][S_pad] rowsum(dO*O)
+  bf16* dq;
+  bf16* dk;
+  bf16* dv;
+  int64_t S, S_pad;
+  int hq, hkv, G, n_tiles;
+  float scale, scale_log2;
+  unsigned* status;
+};
+
+__device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
+  if (t >= p.S) return -1;
+  const int d = __ldg(p.doc + t);
+  if (d < 0) return -1;
+  return p.cu ? (int64_t)__ldg(p.cu + d) : 0;
+}
+__device__ __forceinline__ int64_t doc_end_of(const Params& p, int64_t t) {
+  if (t >= p.S) return -1;
+  const int d = __ldg(p.doc + t);
+  if (d < 0) return -1;
+  return p.cu ? (int64_t)__ldg(p.cu + d + 1) : p.S;
+}
+
+template <int D>
+__device__ __forceinline__ void init_common(Bars* bars) {
+  using C = Cfg<D>;
+  tc::mbar_init(&bars->fix_full, 1);
+  for (int s = 0; s < C::NSTAGE; ++s) {
+    tc::mbar_init(&bars->ring_full[s], 1);
+    tc::mbar_init(&bars->ring_empty[s], 1);
+  }
+  tc::mbar_init(&bars->s_full, 1);
+  tc::mbar_init(&bars->dp_full, 1);
+  tc::mbar_init(&bars->p_full, 128);
+  tc::mbar_init(&bars->mma_done, 1);
+  tc::mbar_init(&bars->drain, 1);
+  bars->abort = 0;
+  tc::fence_mbar_init();
+}
+
+// Producer: two stationary tiles (fixed coordinates) then `n_it` iterations
+// of two streamed tiles each through the ring.  coord(it, w) gives the
+// (c0, c1) of streamed tile w of iteration it; maps[w] its tensor map.
+template <int D, typename CoordFn>
+__device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int* abort,
+                                        const CUtensorMap* f0, int f0c0, const CUtensorMap* f1,
+                                        int f1c0, int fc1, int g, const CUtensorMap* m0,
+                                        const CUtensorMap* m1, int n_it, CoordFn coord) {
+  using C = Cfg<D>;
+  tc::mbar_expect_tx(&bars->fix_full, 2 * C::TILE);
+  for (int b = 0; b < C::NB; ++b) {
+    tc::tma_load_3d(smem + C::FIX_OFF + b * C::BOX, f0, &bars->fix_full, f0c0 + b * 64, fc1, g);
+    tc::tma_load_3d(smem + C::FIX_OFF + C::TILE + b * C::BOX, f1, &bars->fix_full, f1c0 + b * 64,
+                    fc1, g);
+  }
+  int issued = 0;
+  for (int it = 0; it < n_it && !*abort; ++it) {
+    for (int w = 0; w < 2; ++w) {
+      const int idx = 2 * it + w;
+      const int s = idx % C::NSTAGE, use = idx / C::NSTAGE;
+      if (use > 0 && !tc::mbar_wait(&bars->ring_empty[s], (use - 1) & 1, abort)) break;
+      int c0, c1;
+      coord(it, w, c0, c1);
+      tc::mbar_expect_tx(&bars->ring_full[s], C::TILE);
+      for (int b = 0; b < C::NB; ++b)
+        tc::tma_load_3d(smem + C::RING_OFF + s * C::TILE + b * C::BOX, w == 0 ? m0 : m1,
+                        &bars->ring_full[s], c0 + b * 64, c1, g);
+      ++issued;
+    }
+  }
+  if (*abort) {
+    for (int idx = (issued > C::NSTAGE ? issued - C::NSTAGE : 0); idx < issued; ++idx)
+      tc::mbar_wait(&bars->ring_full[idx % C::NSTAGE], (idx / C::NSTAGE) & 1, nullptr,
+                    100000000ull);
+  }
+}
+
+// MMA issuer shared by both kernels.  Per iteration:
+//   T0 = F0 R0^T, T1 = F1 R1^T   (SS: stationary tile F against ring tile R)
+//   then, once the elementwise warps published E0 (over T0) and E1 (over T1):
+//   dkdv:  A0 += E0 R1 (E0 = P^T, R1 = dO),  A1 += E1 R0 (E1 = dS^T, R0 = Q)
+//   dq:    A0 += E0 R0 (E0 = dS,  R0 = K)
+template <int D, bool DKDV>
+__device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int* abort,
+                                         uint32_t tmem, int n_it) {
+  using C = Cfg<D>;
+  constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, A1 = 256 + D;
+  constexpr uint32_t id_st = tc::idesc_bf16(128, BT, false);
+  constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
+  const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
+  const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
+  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort);
+  for (int it = 0; ok && it < n_it; ++it) {
+    const int s0 = (2 * it) % C::NSTAGE, u0 = (2 * it) / C::NSTAGE;
+    const int s1 = (2 * it + 1) % C::NSTAGE, u1 = (2 * it + 1) / C::NSTAGE;
+    if (!(ok = tc::mbar_wait(&bars->ring_full[s0], u0 & 1, abort))) break;
+    if (!(ok = tc::mbar_wait(&bars->ring_full[s1], u1 & 1, abort))) break;
+    if (it > 0 && !(ok = tc::mbar_wait(&bars->mma_done, (it - 1) & 1, abort))) break;
+    tc::fence_after_sync();
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
+      tc::mma_ss(tmem + T0, tc::desc_sw128(fix + off, 16, 1024),
+                 tc::desc_sw128(ring + s0 * C::TILE + off, 16, 1024), id_st, kk > 0);
+    }
+    tc::mma_commit(&bars->s_full);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
+      tc::mma_ss(tmem + T1, tc::desc_sw128(fix + C::TILE + off, 16, 1024),
+                 tc::desc_sw128(ring + s1 * C::TILE + off, 16, 1024), id_st, kk > 0);
+    }
+    tc::mma_commit(&bars->dp_full);
+    if (!(ok = tc::mbar_wait(&bars->p_full, it & 1, abort))) break;
+    tc::fence_after_sync();
+    if (DKDV) {
+#pragma unroll
+      for (int kk = 0; kk < BT / 16; ++kk) {
+        tc::mma_ts(tmem + A0, tmem + T0 + kk * 8,
+                   tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_ts(tmem + A1, tmem + T1 + kk * 8,
+                   tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < BT / 16; ++kk)
+        tc::mma_ts(tmem + A0, tmem + T0 + kk * 8,
+                   tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+    }
+    tc::mma_commit(&bars->mma_done);
+    tc::mma_commit(&bars->ring_empty[s0]);
+    tc::mma_commit(&bars->ring_empty[s1]);
+  }
+  if (!ok) {
+    tc::mma_commit(&bars->drain);
+    tc::mbar_wait(&bars->drain, 0, nullptr, 100000000ull);
+  }
+}
+
+// Store 32 fp32 values (times f) of one row as bf16 to global.
+__device__ __forceinline__ void store_row32(bf16* dst, const uint32_t (&v)[32], float f) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    w[i] = tc::pack_bf16(__uint_as_float(v[2 * i]) * f, __uint_as_float(v[2 * i + 1]) * f);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+
+// ------------------------------------------------------------------- dK, dV
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::BAR_OFF);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int64_t u0 = (int64_t)blockIdx.x * BT;
+  const int g = blockIdx.y / p.hkv;
+  const int jk = blockIdx.y % p.hkv;
+  // query rows that see these keys: [u0, end of the last valid key's document)
+  int n_q = 0;
+  int64_t tq0 = 0;
+  {
+    const int64_t last = min(u0 + BT, p.S) - 1;
+    if (last >= u0) {
+      const int64_t e = doc_end_of(p, last);
+      tq0 = (u0 / BT) * BT;
+      n_q = (int)((e - tq0 + BT - 1) / BT);
+    }
+  }
+  const int n_it = n_q * p.G;    // iteration it: query tile it / G, head jk*G + it % G
+
+  if (threadIdx.x == 0) init_common<D>(bars);
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0 && n_it > 0) {
+      tc::prefetch_tmap(&tmQ);
+      tc::prefetch_tmap(&tmdO);
+      const int G = p.G;
+      produce<D>(smem, bars, abort, &tmK, jk * D, &tmV, jk * D, (int)u0, g, &tmQ, &tmdO, n_it,
+                 [&](int it, int, int& c0, int& c1) {
+                   c0 = (jk * G + it % G) * D;
+                   c1 = (int)(tq0 + (int64_t)(it / G) * BT);
+                 });
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_it > 0) mma_loop<D, true>(smem, bars, abort, tmem, n_it);
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int64_t u = u0 + r;
+    const int64_t de = doc_end_of(p, u);         // queries [u, de) see key u
+    const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
+    const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int64_t t0 = tq0 + (int64_t)(it / p.G) * BT;
+      const int jq = jk * p.G + it % p.G;
+      // per-query LSE*log2(e) and delta of this tile; the arrays carry BT
+      // spare entries so the last tile's columns past S_pad stay in bounds
+      const float* lse2 = p.lse2 + ((int64_t)g * p.hq + jq) * p.S_pad + t0;
+      const float* dl = p.delta + ((int64_t)g * p.hq + jq) * p.S_pad + t0;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->s_full, it & 1, abort) &&
+                                       tc::mbar_wait(&bars->dp_full, it & 1, abort));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const int lo = (int)max((int64_t)0, min((int64_t)BT, u - t0));
+      const int hi = de < 0 ? -1 : (int)min((int64_t)BT - 1, de - 1 - t0);
+      const bool mask = __any_sync(0xffffffffu, lo > 0 || hi < BT - 1);
+#pragma unroll
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t sv[32], dv[32];
+        tc::tmem_ld_x32(tS + c * 32, sv);
+        tc::tmem_ld_x32(tP + c * 32, dv);
+        float l2[32], d2[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(lse2 + c * 32) + i);
+          const float4 b = __ldg(reinterpret_cast<const float4*>(dl + c * 32) + i);
+          l2[4 * i] = a.x; l2[4 * i + 1] = a.y; l2[4 * i + 2] = a.z; l2[4 * i + 3] = a.w;
+          d2[4 * i] = b.x; d2[4 * i + 1] = b.y; d2[4 * i + 2] = b.z; d2[4 * i + 3] = b.w;
+        }
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int k = 2 * i + e;
+            const int col = c * 32 + k;
+            float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), p.scale_log2, -l2[k]));
+            float dsv = pv * (__uint_as_float(dv[k]) - d2[k]);
+            if (mask && (col < lo || col > hi)) { pv = 0.f; dsv = 0.f; }
+            pp[e] = pv;
+            dd[e] = dsv;
+          }
+          pw[i] = tc::pack_bf16(pp[0], pp[1]);
+          dw[i] = tc::pack_bf16(dd[0], dd[1]);
+        }
+        tc::tmem_st_x16(tS + c * 16, pw);
+        tc::tmem_st_x16(tP + c * 16, dw);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->p_full);
+    }
+    if (ok && n_it > 0) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->mma_done, (n_it - 1) & 1, abort));
+      tc::fence_after_sync();
+    }
+    const bool have = ok && n_it > 0;          // warp-uniform
+    bf16* dvrow = p.dv + (((int64_t)g * p.S_pad + u) * p.hkv + jk) * D;
+    bf16* dkrow = p.dk + (((int64_t)g * p.S_pad + u) * p.hkv + jk) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      if (have) {
+        tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + c * 32), v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      if (u < p.S_pad) store_row32(dvrow + c * 32, v, 1.f);
+      if (have) tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + D + c * 32), v);
+      if (u < p.S_pad) store_row32(dkrow + c * 32, v, p.scale);
+    }
+  }
+  __syncwarp();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) usp::set_status(p.status, usp::kErrTimeout);
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ----------------------------------------------------------------------- dQ
+template <int D>
+__global__ void __launch_bounds__(256, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+              const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::BAR_OFF);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int qt = p.n_tiles - 1 - (int)blockIdx.x;
+  const int64_t t0 = (int64_t)qt * BT;
+  const int g = blockIdx.y / p.hq;
+  const int jq = blockIdx.y % p.hq;
+  const int jk = jq / p.G;
+  int n_kv = 0;
+  int64_t kv_start = 0;
+  {
+    const int64_t ds0 = doc_start_of(p, t0);
+    if (ds0 >= 0) {
+      kv_start = (ds0 / BT) * BT;
+      n_kv = (int)((min(t0 + BT, p.S) - kv_start + BT - 1) / BT);
+    }
+  }
+
+  if (threadIdx.x == 0) init_common<D>(bars);
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0 && n_kv > 0) {
+      tc::prefetch_tmap(&tmK);
+      tc::prefetch_tmap(&tmV);
+      produce<D>(smem, bars, abort, &tmQ, jq * D, &tmdO, jq * D, (int)t0, g, &tmK, &tmV, n_kv,
+                 [&](int it, int, int& c0, int& c1) {
+                   c0 = jk * D;
+                   c1 = (int)(kv_start + (int64_t)it * BT);
+                 });
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_kv > 0) mma_loop<D, false>(smem, bars, abort, tmem, n_kv);
+  } else if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int64_t t = t0 + r;
+    const int64_t ds = doc_start_of(p, t);
+    float lse2 = INFINITY, dl = 0.f;
+    if (ds >= 0) {
+      const int64_t li = ((int64_t)g * p.hq + jq) * p.S_pad + t;
+      lse2 = __ldg(p.lse2 + li);
+      dl = __ldg(p.delta + li);
+    }
+    const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
+    const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
+    bool ok = true;
+    for (int it = 0; it < n_kv; ++it) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->s_full, it & 1, abort) &&
+                                       tc::mbar_wait(&bars->dp_full, it & 1, abort));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const int64_t u0 = kv_start + (int64_t)it * BT;
+      const int lo = (int)max((int64_t)0, min((int64_t)BT, ds - u0));
+      const int hi = ds < 0 ? -1 : (int)min((int64_t)BT - 1, t - u0);
+      const bool mask = __any_sync(0xffffffffu, lo > 0 || hi < BT - 1);
+#pragma unroll
+      for (int c = 0; c < BT / 32; ++c) {
+        uint32_t sv[32], dv[32];
+        tc::tmem_ld_x32(tS + c * 32, sv);
+        tc::tmem_ld_x32(tP + c * 32, dv);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = c * 32 + 2 * i + e;
+            float pv = tc::ex2(fmaf(__uint_as_float(sv[2 * i + e]), p.scale_log2, -lse2));
+            float dsv = pv * (__uint_as_float(dv[2 * i + e]) - dl);
+            if (mask && (col < lo || col > hi)) dsv = 0.f;
+            dd[e] = dsv;
+          }
+          w[i] = tc::pack_bf16(dd[0], dd[1]);
+        }
+        tc::tmem_st_x16(tS + c * 16, w);
+      }
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->p_full);
+    }
+    if (ok && n_kv > 0) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->mma_done, (n_kv - 1) & 1, abort));
+      tc::fence_after_sync();
+    }
+    const bool have = ok && n_kv > 0;
+    bf16* row = p.dq + (((int64_t)g * p.S_pad + t) * p.hq + jq) * D;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t v[32];
+      if (have) tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + c * 32), v);
+      else
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      if (t < p.S_pad) store_row32(row + c * 32, v, ds >= 0 ? p.scale : 0.f);
+    }
+  }
+  __syncwarp();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) usp::set_status(p.status, usp::kErrTimeout);
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------ delta = rowsum(dO*O)
+// One warp per (row, head): 16-byte loads, fp32 products and a shuffle sum.
+// Also writes lse2 = LSE*log2(e) (+inf where LSE = -inf) next to it, and
+// zeroes the BT spare entries after both arrays.
+template <int D>
+__global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
+                                                    const bf16* __restrict__ dout,
+                                                    const float* __restrict__ lse,
+                                                    float* __restrict__ delta,
+                                                    float* __restrict__ lse2, int64_t S_pad,
+                                                    int hq, int64_t n_rows) {
+  if (blockIdx.x == 0 && threadIdx.x < BT) {
+    delta[n_rows + threadIdx.x] = 0.f;
+    lse2[n_rows + threadIdx.x] = INFINITY;
+  }
+  constexpr int LPR = D / 8;                  // lanes per row (8 bf16 each)
+  constexpr int RPW = 32 / LPR;               // rows per warp step
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t base = w0 * RPW; base < n_rows; base += nw * RPW) {
+    const int64_t row = base + lane / LPR;    // row = (g*S_pad + t)*hq + j
+    float s = 0.f;
+    if (row < n_rows) {
+      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(o + row * D) + lane % LPR);
+      const uint4 b = __ldcs(reinterpret_cast<const uint4*>(dout + row * D) + lane % LPR);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 fa = __bfloat1622float2(pa[i]);
+        const float2 fb = __bfloat1622float2(pb[i]);
+        s = fmaf(fa.x, fb.x, s);
+        s = fmaf(fa.y, fb.y, s);
+      }
+    }
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (row < n_rows && lane % LPR == 0) {
+      const int64_t gt = row / hq;
+      const int j = (int)(row - gt * hq);
+      const int64_t g = gt / S_pad, t = gt - g * S_pad;
+      const int64_t li = (g * hq + j) * S_pad + t;
+      delta[li] = s;
+      const float x = lse[li];
+      lse2[li] = x == -INFINITY ? INFINITY : x * kLog2e;
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const CUtensorMap& mdo, const Params& prm,
+                       const bf16* o, const bf16* dout, const float* lse, float* delta,
+                       float* lse2, cudaStream_t st) {
+  using C = Cfg<D>;
+  const int64_t n_rows = (int64_t)g.P * g.S_pad * g.hq;
+  int64_t blocks = (n_rows * (D / 8) * 1 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  delta_kernel<D><<<(int)(blocks < 1 ? 1 : blocks), 256, 0, st>>>(o, dout, lse, delta, lse2,
+                                                                 g.S_pad, g.hq, n_rows);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::SMEM)) != cudaSuccess)
+    return e;
+  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), 256, C::SMEM, st>>>(
+      mq, mk, mv, mdo, prm);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), 256, C::SMEM, st>>>(
+      mq, mk, mv, mdo, prm);
+  usp_count_launches(3);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Workspace: delta and lse2, each [P][hq][S_pad] fp32 plus BT spare entries.
+static size_t vec_bytes(const usp::Geometry& g) {
+  const size_t n = ((size_t)g.P * g.hq * g.S_pad + BT) * sizeof(float);
+  return ((n + 255) / 256) * 256;
+}
+size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g) { return 2 * vec_bytes(g); }
+
+cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const void* k,
+                                const void* v, const void* o, const float* lse,
+                                const void* dout, const int32_t* doc, const int32_t* cu,
+                                void* dq, void* dk, void* dv, void* ws, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!usp_make_head_map(&mq, q, g.hq, g.D, g.S_pad, g.P, 128) ||
+      !usp_make_head_map(&mk, k, g.hkv, g.D, g.S_pad, g.P, 128) ||
+      !usp_make_head_map(&mv, v, g.hkv, g.D, g.S_pad, g.P, 128) ||
+      !usp_make_head_map(&mdo, dout, g.hq, g.D, g.S_pad, g.P, 128))
+    return cudaErrorInvalidValue;
+  Params prm;
+  prm.doc = doc;
+  prm.cu = cu;
+  float* delta = reinterpret_cast<float*>(ws);
+  float* lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + vec_bytes(g));
+  prm.lse2 = lse2;
+  prm.delta = delta;
+  prm.dq = reinterpret_cast<bf16*>(dq);
+  prm.dk = reinterpret_cast<bf16*>(dk);
+  prm.dv = reinterpret_cast<bf16*>(dv);
+  prm.S = g.S;
+  prm.S_pad = g.S_pad;
+  prm.hq = g.hq;
+  prm.hkv = g.hkv;
+  prm.G = g.G;
+  prm.n_tiles = (int)((g.S_pad + BT - 1) / BT);
+  prm.scale = g.scale;
+  prm.scale_log2 = g.scale * kLog2e;
+  prm.status = g.status;
+  const bf16* ob = reinterpret_cast<const bf16*>(o);
+  const bf16* db = reinterpret_cast<const bf16*>(dout);
+  if (g.D == 128) return launch_all<128>(g, mq, mk, mv, mdo, prm, ob, db, lse, delta, lse2, st);
+  return launch_all<64>(g, mq, mk, mv, mdo, prm, ob, db, lse, delta, lse2, st);
+}
