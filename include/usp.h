@@ -164,8 +164,8 @@ usp_status usp_attn_bwd(const usp_dims* dims, const void* q_h, const void* k_h,
                         void* dv_h, void* workspace, size_t ws_bytes, void* stream);
 
 /* Bytes of workspace usp_attn_bwd needs for dims: two fp32 arrays of
- * P*(Hq/P)*S_pad + 128 entries (delta_t and LSE_t*log2(e)), each rounded up
- * to 256 bytes.  Returns 0 for invalid dims. */
+ * P*(Hq/P) rows of ceil(S_pad/128)*128 entries (delta_t and LSE_t*log2(e)),
+ * each rounded up to 256 bytes.  Returns 0 for invalid dims. */
 size_t usp_attn_bwd_workspace(const usp_dims* dims);
 
 /*

@@ -60,12 +60,12 @@ struct Bars {
 struct Params {
   const int32_t* doc;
   const int32_t* cu;
-  const float* lse2;     // [P][hq][S_pad] LSE*log2(e); +inf for rows without keys
-  const float* delta;    // [P][hq][S_pad] rowsum(dO*O)
+  const float* lse2;     // [P][hq][S_ws] LSE*log2(e); +inf for rows without keys
+  const float* delta;    // [P][hq][S_ws] rowsum(dO*O); S_ws = S_pad rounded up to BT
   bf16* dq;
   bf16* dk;
   bf16* dv;
-  int64_t S, S_pad;
+  int64_t S, S_pad, S_ws;
   int hq, hkv, G, n_tiles;
   float scale, scale_log2;
   unsigned* status;
@@ -278,10 +278,11 @@ __global__ void __launch_bounds__(256, 1)
     for (int it = 0; it < n_it; ++it) {
       const int64_t t0 = tq0 + (int64_t)(it / p.G) * BT;
       const int jq = jk * p.G + it % p.G;
-      // per-query LSE*log2(e) and delta of this tile; the arrays carry BT
-      // spare entries so the last tile's columns past S_pad stay in bounds
-      const float* lse2 = p.lse2 + ((int64_t)g * p.hq + jq) * p.S_pad + t0;
-      const float* dl = p.delta + ((int64_t)g * p.hq + jq) * p.S_pad + t0;
+      // per-query LSE*log2(e) and delta of this tile: rows of S_ws (a
+      // multiple of BT) entries, so these 16-byte loads are aligned and the
+      // last tile's columns past S_pad read the filled pad entries
+      const float* lse2 = p.lse2 + ((int64_t)g * p.hq + jq) * p.S_ws + t0;
+      const float* dl = p.delta + ((int64_t)g * p.hq + jq) * p.S_ws + t0;
       ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->s_full, it & 1, abort) &&
                                        tc::mbar_wait(&bars->dp_full, it & 1, abort));
       if (!ok) break;
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(256, 1)
     const int64_t ds = doc_start_of(p, t);
     float lse2 = INFINITY, dl = 0.f;
     if (ds >= 0) {
-      const int64_t li = ((int64_t)g * p.hq + jq) * p.S_pad + t;
+      const int64_t li = ((int64_t)g * p.hq + jq) * p.S_ws + t;
       lse2 = __ldg(p.lse2 + li);
       dl = __ldg(p.delta + li);
     }
@@ -484,18 +485,25 @@ __global__ void __launch_bounds__(256, 1)
 
 // ------------------------------------------------------ delta = rowsum(dO*O)
 // One warp per (row, head): 16-byte loads, fp32 products and a shuffle sum.
-// Also writes lse2 = LSE*log2(e) (+inf where LSE = -inf) next to it, and
-// zeroes the BT spare entries after both arrays.
+// Also writes lse2 = LSE*log2(e) (+inf where LSE = -inf).  Both arrays have
+// rows of S_ws >= S_pad entries; entries [S_pad, S_ws) get delta 0, lse2 +inf.
 template <int D>
 __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
                                                     const bf16* __restrict__ dout,
                                                     const float* __restrict__ lse,
                                                     float* __restrict__ delta,
                                                     float* __restrict__ lse2, int64_t S_pad,
-                                                    int hq, int64_t n_rows) {
-  if (blockIdx.x == 0 && threadIdx.x < BT) {
-    delta[n_rows + threadIdx.x] = 0.f;
-    lse2[n_rows + threadIdx.x] = INFINITY;
+                                                    int64_t S_ws, int hq, int64_t n_rows) {
+  {
+    const int64_t extra = S_ws - S_pad;
+    const int64_t n_extra = (n_rows / S_pad) * extra;     // (P*hq) rows
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_extra;
+         i += (int64_t)gridDim.x * blockDim.x) {
+      const int64_t rr = i / extra;
+      const int64_t idx = rr * S_ws + S_pad + (i - rr * extra);
+      delta[idx] = 0.f;
+      lse2[idx] = INFINITY;
+    }
   }
   constexpr int LPR = D / 8;                  // lanes per row (8 bf16 each)
   constexpr int RPW = 32 / LPR;               // rows per warp step
@@ -524,9 +532,9 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
       const int64_t gt = row / hq;
       const int j = (int)(row - gt * hq);
       const int64_t g = gt / S_pad, t = gt - g * S_pad;
-      const int64_t li = (g * hq + j) * S_pad + t;
+      const int64_t li = (g * hq + j) * S_ws + t;
       delta[li] = s;
-      const float x = lse[li];
+      const float x = lse[(g * hq + j) * S_pad + t];
       lse2[li] = x == -INFINITY ? INFINITY : x * kLog2e;
     }
   }
@@ -542,7 +550,7 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
   int64_t blocks = (n_rows * (D / 8) * 1 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   delta_kernel<D><<<(int)(blocks < 1 ? 1 : blocks), 256, 0, st>>>(o, dout, lse, delta, lse2,
-                                                                 g.S_pad, g.hq, n_rows);
+                                                                 g.S_pad, prm.S_ws, g.hq, n_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if ((e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -562,9 +570,11 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
 
 }  // namespace
 
-// Workspace: delta and lse2, each [P][hq][S_pad] fp32 plus BT spare entries.
+// Workspace: delta and lse2, each [P][hq][S_ws] fp32 with S_ws = S_pad
+// rounded up to a multiple of BT.
+static int64_t ws_row(const usp::Geometry& g) { return (g.S_pad + BT - 1) / BT * BT; }
 static size_t vec_bytes(const usp::Geometry& g) {
-  const size_t n = ((size_t)g.P * g.hq * g.S_pad + BT) * sizeof(float);
+  const size_t n = (size_t)g.P * g.hq * ws_row(g) * sizeof(float);
   return ((n + 255) / 256) * 256;
 }
 size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g) { return 2 * vec_bytes(g); }
@@ -591,6 +601,7 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
   prm.dv = reinterpret_cast<bf16*>(dv);
   prm.S = g.S;
   prm.S_pad = g.S_pad;
+  prm.S_ws = ws_row(g);
   prm.hq = g.hq;
   prm.hkv = g.hkv;
   prm.G = g.G;
