@@ -11,6 +11,7 @@ from oracle import usp_oracle as O
 # Tolerances (the same everywhere):
 O_MAX, O_MEAN = 2e-2, 2e-3          # attention output vs fp64
 GRAD_REL = 5e-2                     # dQ/dK/dV max|diff| / max|ref| per tensor
+GRAD_ABS_FLOOR = 1e-4               # when the exact gradient is identically 0
 LSE_ABS = 1e-3
 
 
@@ -33,9 +34,14 @@ def check_o(got, ref, what="O"):
 
 
 def check_grad(got, ref, what):
-    scale = max(np.abs(ref).max(), 1e-30)
-    err = np.abs(got - ref).max() / scale
-    assert err <= GRAD_REL, (what, err)
+    """max|got - ref| <= GRAD_REL * max|ref|.  When the exact gradient is
+    identically zero (e.g. one token per document: softmax over a single key
+    has zero gradient w.r.t. its score) the relative criterion is empty; the
+    GPU then keeps the residue of delta = dO.O computed with bf16 O, and
+    GRAD_ABS_FLOOR bounds it."""
+    err = np.abs(got - ref).max()
+    bound = max(GRAD_REL * np.abs(ref).max(), GRAD_ABS_FLOOR)
+    assert err <= bound, (what, err, bound)
     return err
 
 
