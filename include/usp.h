@@ -163,6 +163,32 @@ usp_status usp_attn_bwd(const usp_dims* dims, const void* q_h, const void* k_h,
                         const void* do_h, const int32_t* doc, void* dq_h, void* dk_h,
                         void* dv_h, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * usp_attn_bwd_noalloc -- usp_attn_bwd for callers that cannot allocate
+ * device memory when they call it: for example a serving process whose
+ * caching allocator reserved the device memory up front, or a runtime whose
+ * policy forbids cudaMalloc after start-up (it synchronises the device and
+ * can fail once memory is exhausted or fragmented).  The pages have no
+ * counterpart; this is a convenience of this library.
+ *
+ * Same arguments, results and errors as usp_attn_bwd, minus the workspace:
+ * the scratch lives in one fixed 32 MiB device array inside the library
+ * (held by every GPU that loads the library until the process exits).  The
+ * call allocates nothing and calls no allocating routine.
+ *   - Limit: usp_attn_bwd_workspace(dims) must be <= 32 MiB, i.e.
+ *     P * (Hq/P) * ceil(S_pad/128)*128 <= 4194304; larger problems return
+ *     USP_ERR_UNSUPPORTED before anything touches the device.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the array.  Calls that overlap on the GPU (other
+ *     streams, other host threads, other devices' calls are fine) race on it
+ *     and give wrong gradients; order them on one stream.
+ */
+usp_status usp_attn_bwd_noalloc(const usp_dims* dims, const void* q_h, const void* k_h,
+                                const void* v_h, const void* o_h, const float* lse,
+                                const void* do_h, const int32_t* doc, void* dq_h, void* dk_h,
+                                void* dv_h, void* stream);
+
 /* Bytes of workspace usp_attn_bwd needs for dims: two fp32 arrays of
  * P*(Hq/P) rows of ceil(S_pad/128)*128 entries (delta_t and LSE_t*log2(e)),
  * each rounded up to 256 bytes.  Returns 0 for invalid dims. */

@@ -53,6 +53,7 @@ _SIGS = {
     "usp_seq_to_head_rope": [_DIMS, _P, _I32, _P, _P, _I64, _I32, _P, _P],
     "usp_attn_fwd": [_DIMS, _P, _P, _P, _P, _P, _P, _P],
     "usp_attn_bwd": [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "usp_attn_bwd_noalloc": [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "usp_head_to_seq": [_DIMS, _P, _I32, _P, _P, _I64, _I32, _P, _P],
     "usp_rope_table": [_I64, _I32, ctypes.c_double, ctypes.c_double, _I32, _P],
     "usp_device_status": [_P],
@@ -144,6 +145,16 @@ def usp_attn_bwd(dims, q_h, k_h, v_h, o_h, lse, do_h, doc, dq_h, dk_h, dv_h, wor
                              _ptr(lse), _ptr(do_h), _ptr(doc), _ptr(dq_h), _ptr(dk_h),
                              _ptr(dv_h), _ptr(workspace), int(ws_bytes), _stream(stream)),
            "usp_attn_bwd")
+
+
+def usp_attn_bwd_noalloc(dims, q_h, k_h, v_h, o_h, lse, do_h, doc, dq_h, dk_h, dv_h,
+                         stream=None):
+    """usp_attn_bwd without a workspace argument (fixed scratch inside the
+    library; see include/usp.h for the size limit and the sharing rules)."""
+    _check(_lib.usp_attn_bwd_noalloc(ctypes.byref(dims), _ptr(q_h), _ptr(k_h), _ptr(v_h),
+                                     _ptr(o_h), _ptr(lse), _ptr(do_h), _ptr(doc), _ptr(dq_h),
+                                     _ptr(dk_h), _ptr(dv_h), _stream(stream)),
+           "usp_attn_bwd_noalloc")
 
 
 def usp_head_to_seq(dims, x_head, H, pos, rope_cs, rope_len, rope_mode, x_seq, stream=None):

@@ -614,3 +614,33 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
   if (g.D == 128) return launch_all<128>(g, mq, mk, mv, mdo, prm, ob, db, lse, delta, lse2, st);
   return launch_all<64>(g, mq, mk, mv, mdo, prm, ob, db, lse, delta, lse2, st);
 }
+
+// ---------------------------------------------------------------------------
+// Fixed scratch for usp_attn_bwd_noalloc: callers that cannot allocate device
+// memory get the backward's workspace (delta and LSE*log2(e)) from this array
+// instead.  Every GPU that loads the library holds it until the process
+// exits.  All calls share it and it keeps the last call's contents; the
+// backward rewrites every entry it reads, so nothing has to be cleared
+// between calls, but calls that overlap on the GPU race on it.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+size_t usp_noalloc_scratch_capacity() { return kNoAllocScratchBytes; }
+
+// Device address of the scratch array on the current device.  The first
+// call on a device looks it up (with that device current) and caches it.
+cudaError_t usp_noalloc_scratch(void** ptr) {
+  static void* cache[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev] = p;
+  }
+  *ptr = cache[dev];
+  return cudaSuccess;
+}

@@ -202,6 +202,28 @@ usp_status usp_attn_bwd(const usp_dims* dims, const void* q_h, const void* k_h,
                                          (cudaStream_t)stream));
 }
 
+usp_status usp_attn_bwd_noalloc(const usp_dims* dims, const void* q_h, const void* k_h,
+                                const void* v_h, const void* o_h, const float* lse,
+                                const void* do_h, const int32_t* doc, void* dq_h, void* dk_h,
+                                void* dv_h, void* stream) {
+  usp::Geometry g;
+  usp_status s = geometry(dims, &g);
+  if (s != USP_OK) return s;
+  const void* ptrs[] = {q_h, k_h, v_h, o_h, lse, do_h, dq_h, dk_h, dv_h};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return USP_ERR_INVALID_ARG;
+  if (doc == nullptr || ((uintptr_t)doc & 3u)) return USP_ERR_INVALID_ARG;
+  if (g.S_pad == 0) return USP_OK;
+  // size limit first: nothing touches the device for a problem that does not fit
+  if (usp_attn_bwd_ws_bytes(g) > usp_noalloc_scratch_capacity()) return USP_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (usp_noalloc_scratch(&scratch) != cudaSuccess || scratch == nullptr) return USP_ERR_CUDA;
+  if ((g.status = status_word()) == nullptr) return USP_ERR_CUDA;
+  return cuda_status(usp_launch_attn_bwd(g, q_h, k_h, v_h, o_h, lse, do_h, doc,
+                                         dims->cu_seqlens, dq_h, dk_h, dv_h, scratch,
+                                         (cudaStream_t)stream));
+}
+
 usp_status usp_rope_table(int64_t n_pos, int32_t D, double base, double yarn_factor,
                           int32_t yarn_orig_ctx, float* out_host) {
   if (n_pos < 0 || D < 2 || (D & 1) || out_host == nullptr || !(base > 1.0))

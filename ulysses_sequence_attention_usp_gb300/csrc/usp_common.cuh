@@ -49,6 +49,10 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
                                 void* dq, void* dk, void* dv, void* ws, cudaStream_t st);
 size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g);
 
+// Fixed backward scratch for usp_attn_bwd_noalloc (attn_bwd_tc.cu).
+size_t usp_noalloc_scratch_capacity();
+cudaError_t usp_noalloc_scratch(void** ptr);
+
 // Tensor map (TMA descriptor) over a head-layout bf16 tensor [P][S_pad][heads][D],
 // boxes of 64 columns x box_rows rows with 128-byte swizzle (attn_fwd_tc.cu).
 struct CUtensorMap_st;
