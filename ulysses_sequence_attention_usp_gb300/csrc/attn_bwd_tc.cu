@@ -21,8 +21,13 @@
 //                 key tiles:  S = Q K^T, dP = dO V^T (SS), dS over S (bf16),
 //                 dQ += dS K (TS).
 // Both reuse the forward's warp roles: warp 0 TMA producer, warp 1 TMEM
-// owner and MMA issuer, warps 4-7 the per-row elementwise work and the
-// epilogue.  All waits are bounded (status word on timeout).
+// owner and MMA issuer; warps 4-7 and 8-11 do the per-row elementwise work
+// on the left and right 64 columns of each tile (two warps per SM
+// sub-partition, so one hides the other's latency) and the epilogue.
+// The bf16 values of each 32-column chunk are written over the first 16
+// TMEM columns of that same chunk, so the two halves never touch each
+// other's columns; the TS MMAs address K-step kk at column
+// 32*(kk/2) + 8*(kk%2).  All waits are bounded (status word on timeout).
 #include "tc_ptx.cuh"
 #include "usp_common.cuh"
 
@@ -94,7 +99,7 @@ __device__ __forceinline__ void init_common(Bars* bars) {
   }
   tc::mbar_init(&bars->s_full, 1);
   tc::mbar_init(&bars->dp_full, 1);
-  tc::mbar_init(&bars->p_full, 128);
+  tc::mbar_init(&bars->p_full, 256);
   tc::mbar_init(&bars->mma_done, 1);
   tc::mbar_init(&bars->drain, 1);
   bars->abort = 0;
@@ -179,17 +184,18 @@ __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int
     if (DKDV) {
 #pragma unroll
       for (int kk = 0; kk < BT / 16; ++kk) {
-        tc::mma_ts(tmem + A0, tmem + T0 + kk * 8,
+        const uint32_t ka = 32 * (kk >> 1) + 8 * (kk & 1);
+        tc::mma_ts(tmem + A0, tmem + T0 + ka,
                    tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                    (it > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_ts(tmem + A1, tmem + T1 + kk * 8,
+        tc::mma_ts(tmem + A1, tmem + T1 + ka,
                    tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                    (it > 0 || kk > 0) ? 1u : 0u);
       }
     } else {
 #pragma unroll
       for (int kk = 0; kk < BT / 16; ++kk)
-        tc::mma_ts(tmem + A0, tmem + T0 + kk * 8,
+        tc::mma_ts(tmem + A0, tmem + T0 + 32 * (kk >> 1) + 8 * (kk & 1),
                    tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                    (it > 0 || kk > 0) ? 1u : 0u);
     }
@@ -201,6 +207,75 @@ __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int
     tc::mma_commit(&bars->drain);
     tc::mbar_wait(&bars->drain, 0, nullptr, 100000000ull);
   }
+}
+
+// dK/dV elementwise work on one 32-column chunk c of this thread's key row:
+// P^T = exp2(S^T*sl2 - lse2[col]), dS^T = P^T (dP^T - delta[col]); both
+// written as bf16 over the chunk's first 16 columns.  Columns outside
+// [lo, hi] are zero when MASK.
+template <bool MASK>
+__device__ __forceinline__ void dkdv_chunk(uint32_t tS, uint32_t tP, int c, int lo, int hi,
+                                           const float* lse2, const float* dl, float sl2) {
+  uint32_t sv[32], dv[32];
+  tc::tmem_ld_x32(tS + c * 32, sv);
+  tc::tmem_ld_x32(tP + c * 32, dv);
+  float l2[32], d2[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(lse2 + c * 32) + i);
+    const float4 b = __ldg(reinterpret_cast<const float4*>(dl + c * 32) + i);
+    l2[4 * i] = a.x; l2[4 * i + 1] = a.y; l2[4 * i + 2] = a.z; l2[4 * i + 3] = a.w;
+    d2[4 * i] = b.x; d2[4 * i + 1] = b.y; d2[4 * i + 2] = b.z; d2[4 * i + 3] = b.w;
+  }
+  uint32_t pw[16], dw[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float pp[2], dd[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int k = 2 * i + e;
+      float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -l2[k]));
+      float dsv = pv * (__uint_as_float(dv[k]) - d2[k]);
+      if (MASK) {
+        const int col = c * 32 + k;
+        if (!(col >= lo && col <= hi)) { pv = 0.f; dsv = 0.f; }
+      }
+      pp[e] = pv;
+      dd[e] = dsv;
+    }
+    pw[i] = tc::pack_bf16(pp[0], pp[1]);
+    dw[i] = tc::pack_bf16(dd[0], dd[1]);
+  }
+  tc::tmem_st_x16(tS + c * 32, pw);
+  tc::tmem_st_x16(tP + c * 32, dw);
+}
+
+// dQ elementwise work on chunk c of this thread's query row:
+// dS = exp2(S*sl2 - lse2) (dP - delta), bf16 over the chunk's first 16 columns.
+template <bool MASK>
+__device__ __forceinline__ void dq_chunk(uint32_t tS, uint32_t tP, int c, int lo, int hi,
+                                         float lse2, float dl, float sl2) {
+  uint32_t sv[32], dv[32];
+  tc::tmem_ld_x32(tS + c * 32, sv);
+  tc::tmem_ld_x32(tP + c * 32, dv);
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float dd[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int k = 2 * i + e;
+      const float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -lse2));
+      float dsv = pv * (__uint_as_float(dv[k]) - dl);
+      if (MASK) {
+        const int col = c * 32 + k;
+        if (!(col >= lo && col <= hi)) dsv = 0.f;
+      }
+      dd[e] = dsv;
+    }
+    w[i] = tc::pack_bf16(dd[0], dd[1]);
+  }
+  tc::tmem_st_x16(tS + c * 32, w);
 }
 
 // Store 32 fp32 values (times f) of one row as bf16 to global.
@@ -216,7 +291,7 @@ __device__ __forceinline__ void store_row32(bf16* dst, const uint32_t (&v)[32], 
 
 // ------------------------------------------------------------------- dK, dV
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const Params p) {
@@ -269,6 +344,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0 && n_it > 0) mma_loop<D, true>(smem, bars, abort, tmem, n_it);
   } else if (warp >= 4) {
     const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)
     const int r = quarter * 32 + lane;
     const int64_t u = u0 + r;
     const int64_t de = doc_end_of(p, u);         // queries [u, de) see key u
@@ -289,39 +365,11 @@ __global__ void __launch_bounds__(256, 1)
       tc::fence_after_sync();
       const int lo = (int)max((int64_t)0, min((int64_t)BT, u - t0));
       const int hi = de < 0 ? -1 : (int)min((int64_t)BT - 1, de - 1 - t0);
-      const bool mask = __any_sync(0xffffffffu, lo > 0 || hi < BT - 1);
+      const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
 #pragma unroll
-      for (int c = 0; c < BT / 32; ++c) {
-        uint32_t sv[32], dv[32];
-        tc::tmem_ld_x32(tS + c * 32, sv);
-        tc::tmem_ld_x32(tP + c * 32, dv);
-        float l2[32], d2[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 a = __ldg(reinterpret_cast<const float4*>(lse2 + c * 32) + i);
-          const float4 b = __ldg(reinterpret_cast<const float4*>(dl + c * 32) + i);
-          l2[4 * i] = a.x; l2[4 * i + 1] = a.y; l2[4 * i + 2] = a.z; l2[4 * i + 3] = a.w;
-          d2[4 * i] = b.x; d2[4 * i + 1] = b.y; d2[4 * i + 2] = b.z; d2[4 * i + 3] = b.w;
-        }
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float pp[2], dd[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int k = 2 * i + e;
-            const int col = c * 32 + k;
-            float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), p.scale_log2, -l2[k]));
-            float dsv = pv * (__uint_as_float(dv[k]) - d2[k]);
-            if (mask && (col < lo || col > hi)) { pv = 0.f; dsv = 0.f; }
-            pp[e] = pv;
-            dd[e] = dsv;
-          }
-          pw[i] = tc::pack_bf16(pp[0], pp[1]);
-          dw[i] = tc::pack_bf16(dd[0], dd[1]);
-        }
-        tc::tmem_st_x16(tS + c * 16, pw);
-        tc::tmem_st_x16(tP + c * 16, dw);
+      for (int cc = 0; cc < 2; ++cc) {
+        if (mask) dkdv_chunk<true>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
+        else dkdv_chunk<false>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -331,21 +379,21 @@ __global__ void __launch_bounds__(256, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->mma_done, (n_it - 1) & 1, abort));
       tc::fence_after_sync();
     }
+    // epilogue: the left half writes dV, the right half dK
     const bool have = ok && n_it > 0;          // warp-uniform
-    bf16* dvrow = p.dv + (((int64_t)g * p.S_pad + u) * p.hkv + jk) * D;
-    bf16* dkrow = p.dk + (((int64_t)g * p.S_pad + u) * p.hkv + jk) * D;
+    bf16* row = (half == 0 ? p.dv : p.dk) + (((int64_t)g * p.S_pad + u) * p.hkv + jk) * D;
+    const uint32_t acc = 256 + half * D;
+    const float f = half == 0 ? 1.f : p.scale;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];
       if (have) {
-        tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + c * 32), v);
+        tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, acc + c * 32), v);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
       }
-      if (u < p.S_pad) store_row32(dvrow + c * 32, v, 1.f);
-      if (have) tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + D + c * 32), v);
-      if (u < p.S_pad) store_row32(dkrow + c * 32, v, p.scale);
+      if (u < p.S_pad) store_row32(row + c * 32, v, f);
     }
   }
   __syncwarp();
@@ -360,7 +408,7 @@ __global__ void __launch_bounds__(256, 1)
 
 // ----------------------------------------------------------------------- dQ
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const Params p) {
@@ -411,6 +459,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0 && n_kv > 0) mma_loop<D, false>(smem, bars, abort, tmem, n_kv);
   } else if (warp >= 4) {
     const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)
     const int r = quarter * 32 + lane;
     const int64_t t = t0 + r;
     const int64_t ds = doc_start_of(p, t);
@@ -431,27 +480,11 @@ __global__ void __launch_bounds__(256, 1)
       const int64_t u0 = kv_start + (int64_t)it * BT;
       const int lo = (int)max((int64_t)0, min((int64_t)BT, ds - u0));
       const int hi = ds < 0 ? -1 : (int)min((int64_t)BT - 1, t - u0);
-      const bool mask = __any_sync(0xffffffffu, lo > 0 || hi < BT - 1);
+      const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
 #pragma unroll
-      for (int c = 0; c < BT / 32; ++c) {
-        uint32_t sv[32], dv[32];
-        tc::tmem_ld_x32(tS + c * 32, sv);
-        tc::tmem_ld_x32(tP + c * 32, dv);
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float dd[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c * 32 + 2 * i + e;
-            float pv = tc::ex2(fmaf(__uint_as_float(sv[2 * i + e]), p.scale_log2, -lse2));
-            float dsv = pv * (__uint_as_float(dv[2 * i + e]) - dl);
-            if (mask && (col < lo || col > hi)) dsv = 0.f;
-            dd[e] = dsv;
-          }
-          w[i] = tc::pack_bf16(dd[0], dd[1]);
-        }
-        tc::tmem_st_x16(tS + c * 16, w);
+      for (int cc = 0; cc < 2; ++cc) {
+        if (mask) dq_chunk<true>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
+        else dq_chunk<false>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -464,12 +497,14 @@ __global__ void __launch_bounds__(256, 1)
     const bool have = ok && n_kv > 0;
     bf16* row = p.dq + (((int64_t)g * p.S_pad + t) * p.hq + jq) * D;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
       uint32_t v[32];
-      if (have) tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + c * 32), v);
-      else
+      if (have) {
+        tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + c * 32), v);
+      } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
       if (t < p.S_pad) store_row32(row + c * 32, v, ds >= 0 ? p.scale : 0.f);
     }
   }
@@ -559,10 +594,10 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
   if ((e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::SMEM)) != cudaSuccess)
     return e;
-  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), 256, C::SMEM, st>>>(
+  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), 384, C::SMEM, st>>>(
       mq, mk, mv, mdo, prm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), 256, C::SMEM, st>>>(
+  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), 384, C::SMEM, st>>>(
       mq, mk, mv, mdo, prm);
   usp_count_launches(3);
   return cudaGetLastError();

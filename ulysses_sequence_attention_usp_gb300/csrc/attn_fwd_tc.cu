@@ -82,6 +82,65 @@ __device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
   return p.cu ? (int64_t)__ldg(p.cu + d) : 0;
 }
 
+// Row max of this thread's S row (128 fp32 columns in TMEM).  With MASK the
+// columns outside [lo, hi] count as -inf; without it no column is tested.
+template <bool MASK>
+__device__ __forceinline__ float s_row_max(uint32_t tS, int lo, int hi) {
+  float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t v[32];
+    tc::tmem_ld_x32(tS + c * 32, v);
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        x[e] = __uint_as_float(v[i + e]);
+        if (MASK) {
+          const int col = c * 32 + i + e;
+          if (!(col >= lo && col <= hi)) x[e] = -INFINITY;
+        }
+      }
+      m0 = tc::max3(m0, x[0], x[1]);
+      m1 = tc::max3(m1, x[2], x[3]);
+      m2 = tc::max3(m2, x[4], x[5]);
+      m3 = tc::max3(m3, x[6], x[7]);
+    }
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// P = exp2(S*scale_log2 - m_eff) written as bf16 pairs over the first 64
+// columns of the S row; returns the fp32 row sum.
+template <bool MASK>
+__device__ __forceinline__ float s_row_exp(uint32_t tS, int lo, int hi, float sl2, float m_eff) {
+  float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t v[32];
+    tc::tmem_ld_x32(tS + c * 32, v);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float x0 = __uint_as_float(v[2 * i]);
+      float x1 = __uint_as_float(v[2 * i + 1]);
+      if (MASK) {
+        const int col = c * 32 + 2 * i;
+        if (!(col >= lo && col <= hi)) x0 = -INFINITY;
+        if (!(col + 1 >= lo && col + 1 <= hi)) x1 = -INFINITY;
+      }
+      const float p0 = tc::ex2(fmaf(x0, sl2, -m_eff));
+      const float p1 = tc::ex2(fmaf(x1, sl2, -m_eff));
+      r0 += p0;
+      r1 += p1;
+      w[i] = tc::pack_bf16(p0, p1);
+    }
+    tc::tmem_st_x16(tS + c * 16, w);
+  }
+  return r0 + r1;
+}
+
 template <int D, int NH>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -250,19 +309,9 @@ __global__ void __launch_bounds__(384, 1)
         // keys u0+c visible to row t iff ds <= u0+c <= t  (c in [lo, hi])
         const int lo = (int)max((int64_t)0, min((int64_t)BN, ds - u0));
         const int hi = ds < 0 ? -1 : (int)min((int64_t)BN - 1, t - u0);
-        // pass 1: row max
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tc::tmem_ld_x32(tS + c * 32, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float x = __uint_as_float(v[i]);
-            if (mask && (c * 32 + i < lo || c * 32 + i > hi)) x = -INFINITY;
-            mx = fmaxf(mx, x);
-          }
-        }
+        // pass 1: row max; the mask is warp-uniform, so fully visible tiles
+        // take the path without per-column tests
+        const float mx = mask ? s_row_max<true>(tS, lo, hi) : s_row_max<false>(tS, lo, hi);
         const float m_tile = mx * p.scale_log2;
         const float m_new = fmaxf(m, m_tile);
         const bool rescale = m_new > m + kRescaleThreshold;
@@ -270,28 +319,8 @@ __global__ void __launch_bounds__(384, 1)
         const float alpha = rescale ? tc::ex2(m - m_new) : 1.f;
         const float m_eff = m_use == -INFINITY ? 0.f : m_use;
         // pass 2: P = exp2(S*scale*log2e - m), written as bf16 over S
-        float rowsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tc::tmem_ld_x32(tS + c * 32, v);
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0 = __uint_as_float(v[2 * i]);
-            float x1 = __uint_as_float(v[2 * i + 1]);
-            if (mask) {
-              const int c0 = c * 32 + 2 * i;
-              if (c0 < lo || c0 > hi) x0 = -INFINITY;
-              if (c0 + 1 < lo || c0 + 1 > hi) x1 = -INFINITY;
-            }
-            const float p0 = tc::ex2(fmaf(x0, p.scale_log2, -m_eff));
-            const float p1 = tc::ex2(fmaf(x1, p.scale_log2, -m_eff));
-            rowsum += p0 + p1;
-            w[i] = tc::pack_bf16(p0, p1);
-          }
-          tc::tmem_st_x16(tS + c * 16, w);
-        }
+        const float rowsum = mask ? s_row_exp<true>(tS, lo, hi, p.scale_log2, m_eff)
+                                  : s_row_exp<false>(tS, lo, hi, p.scale_log2, m_eff);
         l = l * alpha + rowsum;
         m = m_use;
         if (jt > 0 && __any_sync(0xffffffffu, rescale)) {
