@@ -46,17 +46,20 @@ struct Cfg {
   static constexpr int FIX_OFF = 0;           // two stationary tiles
   static constexpr int RING_OFF = 2 * TILE;
   static constexpr int BAR_OFF = RING_OFF + NSTAGE * TILE;
-  static constexpr int SMEM = BAR_OFF + 512 + 1024;
+  static constexpr int VEC_OFF = BAR_OFF + 512;   // per ring slot: 128 fp32 (dkdv)
+  static constexpr int SMEM = VEC_OFF + NSTAGE * BT * 4 + 1024;
 };
 
+// Each 128-column tile is processed as two 64-column halves with their own
+// TMEM regions and barriers, so the MMAs of one half run while the
+// elementwise warps work on the other.
 struct Bars {
   uint64_t fix_full;
   uint64_t ring_full[8];
   uint64_t ring_empty[8];
-  uint64_t s_full;
-  uint64_t dp_full;
-  uint64_t p_full;
-  uint64_t mma_done;
+  uint64_t sd_full[2];    // S and dP of half h computed
+  uint64_t p_full[2];     // elementwise of half h published (128 arrivals)
+  uint64_t done[2];       // accumulation MMAs of half h completed
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -97,23 +100,27 @@ __device__ __forceinline__ void init_common(Bars* bars) {
     tc::mbar_init(&bars->ring_full[s], 1);
     tc::mbar_init(&bars->ring_empty[s], 1);
   }
-  tc::mbar_init(&bars->s_full, 1);
-  tc::mbar_init(&bars->dp_full, 1);
-  tc::mbar_init(&bars->p_full, 256);
-  tc::mbar_init(&bars->mma_done, 1);
+  for (int h = 0; h < 2; ++h) {
+    tc::mbar_init(&bars->sd_full[h], 1);
+    tc::mbar_init(&bars->p_full[h], 128);
+    tc::mbar_init(&bars->done[h], 1);
+  }
   tc::mbar_init(&bars->drain, 1);
   bars->abort = 0;
   tc::fence_mbar_init();
 }
 
 // Producer: two stationary tiles (fixed coordinates) then `n_it` iterations
-// of two streamed tiles each through the ring.  coord(it, w) gives the
-// (c0, c1) of streamed tile w of iteration it; maps[w] its tensor map.
-template <int D, typename CoordFn>
+// of two streamed tiles each through the ring.  coord(it, w, c0, c1) gives
+// the coordinates of streamed tile w of iteration it (map m0 or m1).  With
+// VEC, vec(it, w) also names 128 fp32 values copied next to the tile (into
+// the slot's vector area; 512 bytes, 16-byte aligned).
+template <int D, bool VEC, typename CoordFn, typename VecFn>
 __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int* abort,
                                         const CUtensorMap* f0, int f0c0, const CUtensorMap* f1,
                                         int f1c0, int fc1, int g, const CUtensorMap* m0,
-                                        const CUtensorMap* m1, int n_it, CoordFn coord) {
+                                        const CUtensorMap* m1, int n_it, CoordFn coord,
+                                        VecFn vec) {
   using C = Cfg<D>;
   tc::mbar_expect_tx(&bars->fix_full, 2 * C::TILE);
   for (int b = 0; b < C::NB; ++b) {
@@ -129,10 +136,12 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int*
       if (use > 0 && !tc::mbar_wait(&bars->ring_empty[s], (use - 1) & 1, abort)) break;
       int c0, c1;
       coord(it, w, c0, c1);
-      tc::mbar_expect_tx(&bars->ring_full[s], C::TILE);
+      tc::mbar_expect_tx(&bars->ring_full[s], C::TILE + (VEC ? BT * 4 : 0));
       for (int b = 0; b < C::NB; ++b)
         tc::tma_load_3d(smem + C::RING_OFF + s * C::TILE + b * C::BOX, w == 0 ? m0 : m1,
                         &bars->ring_full[s], c0 + b * 64, c1, g);
+      if (VEC)
+        tc::bulk_load(smem + C::VEC_OFF + s * BT * 4, vec(it, w), BT * 4, &bars->ring_full[s]);
       ++issued;
     }
   }
@@ -143,17 +152,22 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int*
   }
 }
 
-// MMA issuer shared by both kernels.  Per iteration:
-//   T0 = F0 R0^T, T1 = F1 R1^T   (SS: stationary tile F against ring tile R)
-//   then, once the elementwise warps published E0 (over T0) and E1 (over T1):
-//   dkdv:  A0 += E0 R1 (E0 = P^T, R1 = dO),  A1 += E1 R0 (E1 = dS^T, R0 = Q)
-//   dq:    A0 += E0 R0 (E0 = dS,  R0 = K)
+// MMA issuer shared by both kernels.  Iteration `it` streams ring tiles R0
+// and R1 against the stationary tiles F0 and F1.  For each half h (rows
+// [64h, 64h+64) of the ring tiles, TMEM columns [64h, 64h+64) of T0/T1):
+//   T0_h = F0 R0_h^T, T1_h = F1 R1_h^T          (SS, M=128 N=64 K=D)
+// and, once the elementwise warps of half h published E0_h (over T0_h) and
+// E1_h (over T1_h), the accumulation over that half's 64 rows (K=64):
+//   dkdv:  A0 += E0_h R1_h (dV += P^T dO),  A1 += E1_h R0_h (dK += dS^T Q)
+//   dq:    A0 += E0_h R0_h (dQ += dS K)
+// T0_h/T1_h are rewritten for iteration it+1 only after done[h] of
+// iteration it, i.e. after the accumulation MMAs that read E0_h/E1_h.
 template <int D, bool DKDV>
 __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int* abort,
                                          uint32_t tmem, int n_it) {
   using C = Cfg<D>;
   constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, A1 = 256 + D;
-  constexpr uint32_t id_st = tc::idesc_bf16(128, BT, false);
+  constexpr uint32_t id_st = tc::idesc_bf16(128, BT / 2, false);
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
@@ -163,43 +177,45 @@ __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int
     const int s1 = (2 * it + 1) % C::NSTAGE, u1 = (2 * it + 1) / C::NSTAGE;
     if (!(ok = tc::mbar_wait(&bars->ring_full[s0], u0 & 1, abort))) break;
     if (!(ok = tc::mbar_wait(&bars->ring_full[s1], u1 & 1, abort))) break;
-    if (it > 0 && !(ok = tc::mbar_wait(&bars->mma_done, (it - 1) & 1, abort))) break;
-    tc::fence_after_sync();
+    for (int h = 0; h < 2 && ok; ++h) {
+      if (it > 0 && !(ok = tc::mbar_wait(&bars->done[h], (it - 1) & 1, abort))) break;
+      tc::fence_after_sync();
+      const uint32_t rows = h * 64 * 128;     // byte offset of row 64h in a box
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
-      tc::mma_ss(tmem + T0, tc::desc_sw128(fix + off, 16, 1024),
-                 tc::desc_sw128(ring + s0 * C::TILE + off, 16, 1024), id_st, kk > 0);
-    }
-    tc::mma_commit(&bars->s_full);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
-      tc::mma_ss(tmem + T1, tc::desc_sw128(fix + C::TILE + off, 16, 1024),
-                 tc::desc_sw128(ring + s1 * C::TILE + off, 16, 1024), id_st, kk > 0);
-    }
-    tc::mma_commit(&bars->dp_full);
-    if (!(ok = tc::mbar_wait(&bars->p_full, it & 1, abort))) break;
-    tc::fence_after_sync();
-    if (DKDV) {
-#pragma unroll
-      for (int kk = 0; kk < BT / 16; ++kk) {
-        const uint32_t ka = 32 * (kk >> 1) + 8 * (kk & 1);
-        tc::mma_ts(tmem + A0, tmem + T0 + ka,
-                   tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_ts(tmem + A1, tmem + T1 + ka,
-                   tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
+        tc::mma_ss(tmem + T0 + 64 * h, tc::desc_sw128(fix + off, 16, 1024),
+                   tc::desc_sw128(ring + s0 * C::TILE + off + rows, 16, 1024), id_st, kk > 0);
       }
-    } else {
 #pragma unroll
-      for (int kk = 0; kk < BT / 16; ++kk)
-        tc::mma_ts(tmem + A0, tmem + T0 + 32 * (kk >> 1) + 8 * (kk & 1),
-                   tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
+        tc::mma_ss(tmem + T1 + 64 * h, tc::desc_sw128(fix + C::TILE + off, 16, 1024),
+                   tc::desc_sw128(ring + s1 * C::TILE + off + rows, 16, 1024), id_st, kk > 0);
+      }
+      tc::mma_commit(&bars->sd_full[h]);
     }
-    tc::mma_commit(&bars->mma_done);
+    for (int h = 0; h < 2 && ok; ++h) {
+      if (!(ok = tc::mbar_wait(&bars->p_full[h], it & 1, abort))) break;
+      tc::fence_after_sync();
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const int kk = 4 * h + k4;             // 16-row K step within the tile
+        const uint32_t ka = 32 * (kk >> 1) + 8 * (kk & 1);
+        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+        if (DKDV) {
+          tc::mma_ts(tmem + A0, tmem + T0 + ka,
+                     tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
+          tc::mma_ts(tmem + A1, tmem + T1 + ka,
+                     tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
+        } else {
+          tc::mma_ts(tmem + A0, tmem + T0 + ka,
+                     tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
+        }
+      }
+      tc::mma_commit(&bars->done[h]);
+    }
+    if (!ok) break;
     tc::mma_commit(&bars->ring_empty[s0]);
     tc::mma_commit(&bars->ring_empty[s1]);
   }
@@ -209,73 +225,79 @@ __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int
   }
 }
 
-// dK/dV elementwise work on one 32-column chunk c of this thread's key row:
-// P^T = exp2(S^T*sl2 - lse2[col]), dS^T = P^T (dP^T - delta[col]); both
-// written as bf16 over the chunk's first 16 columns.  Columns outside
-// [lo, hi] are zero when MASK.
+// dK/dV elementwise work on half h (columns [64h, 64h+64)) of this thread's
+// key row, read from TMEM with one wait:
+//   P^T = exp2(S^T*sl2 - lse2[col]),  dS^T = P^T (dP^T - delta[col]),
+// both written as bf16 over the first 16 columns of each 32-column chunk.
+// Columns outside [lo, hi] are zero when MASK.
 template <bool MASK>
-__device__ __forceinline__ void dkdv_chunk(uint32_t tS, uint32_t tP, int c, int lo, int hi,
-                                           const float* lse2, const float* dl, float sl2) {
-  uint32_t sv[32], dv[32];
-  tc::tmem_ld_x32(tS + c * 32, sv);
-  tc::tmem_ld_x32(tP + c * 32, dv);
-  float l2[32], d2[32];
+__device__ __forceinline__ void dkdv_half(uint32_t tS, uint32_t tP, int h, int lo, int hi,
+                                          const float* lse2, const float* dl, float sl2) {
+  uint32_t sv[64], dv[64];
+  tc::tmem_ld2_x64(tS + 64 * h, tP + 64 * h, sv, dv);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float4 a = __ldg(reinterpret_cast<const float4*>(lse2 + c * 32) + i);
-    const float4 b = __ldg(reinterpret_cast<const float4*>(dl + c * 32) + i);
-    l2[4 * i] = a.x; l2[4 * i + 1] = a.y; l2[4 * i + 2] = a.z; l2[4 * i + 3] = a.w;
-    d2[4 * i] = b.x; d2[4 * i + 1] = b.y; d2[4 * i + 2] = b.z; d2[4 * i + 3] = b.w;
-  }
-  uint32_t pw[16], dw[16];
+  for (int cc = 0; cc < 2; ++cc) {
+    const int c = 2 * h + cc;
+    uint32_t pw[16], dw[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float pp[2], dd[2];
+    for (int i = 0; i < 8; ++i) {   // shared memory, same address in every lane
+      const float4 a = reinterpret_cast<const float4*>(lse2 + c * 32)[i];
+      const float4 b = reinterpret_cast<const float4*>(dl + c * 32)[i];
+      const float l2[4] = {a.x, a.y, a.z, a.w};
+      const float d2[4] = {b.x, b.y, b.z, b.w};
+      float pp[4], dd[4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int k = 2 * i + e;
-      float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -l2[k]));
-      float dsv = pv * (__uint_as_float(dv[k]) - d2[k]);
-      if (MASK) {
-        const int col = c * 32 + k;
-        if (!(col >= lo && col <= hi)) { pv = 0.f; dsv = 0.f; }
+      for (int e = 0; e < 4; ++e) {
+        const int k = cc * 32 + 4 * i + e;
+        float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -l2[e]));
+        float dsv = pv * (__uint_as_float(dv[k]) - d2[e]);
+        if (MASK) {
+          const int col = c * 32 + 4 * i + e;
+          if (!(col >= lo && col <= hi)) { pv = 0.f; dsv = 0.f; }
+        }
+        pp[e] = pv;
+        dd[e] = dsv;
       }
-      pp[e] = pv;
-      dd[e] = dsv;
+      pw[2 * i] = tc::pack_bf16(pp[0], pp[1]);
+      pw[2 * i + 1] = tc::pack_bf16(pp[2], pp[3]);
+      dw[2 * i] = tc::pack_bf16(dd[0], dd[1]);
+      dw[2 * i + 1] = tc::pack_bf16(dd[2], dd[3]);
     }
-    pw[i] = tc::pack_bf16(pp[0], pp[1]);
-    dw[i] = tc::pack_bf16(dd[0], dd[1]);
+    tc::tmem_st_x16(tS + c * 32, pw);
+    tc::tmem_st_x16(tP + c * 32, dw);
   }
-  tc::tmem_st_x16(tS + c * 32, pw);
-  tc::tmem_st_x16(tP + c * 32, dw);
 }
 
-// dQ elementwise work on chunk c of this thread's query row:
-// dS = exp2(S*sl2 - lse2) (dP - delta), bf16 over the chunk's first 16 columns.
+// dQ elementwise work on half h of this thread's query row:
+// dS = exp2(S*sl2 - lse2) (dP - delta), bf16 over the first 16 columns of
+// each 32-column chunk.
 template <bool MASK>
-__device__ __forceinline__ void dq_chunk(uint32_t tS, uint32_t tP, int c, int lo, int hi,
-                                         float lse2, float dl, float sl2) {
-  uint32_t sv[32], dv[32];
-  tc::tmem_ld_x32(tS + c * 32, sv);
-  tc::tmem_ld_x32(tP + c * 32, dv);
-  uint32_t w[16];
+__device__ __forceinline__ void dq_half(uint32_t tS, uint32_t tP, int h, int lo, int hi,
+                                        float lse2, float dl, float sl2) {
+  uint32_t sv[64], dv[64];
+  tc::tmem_ld2_x64(tS + 64 * h, tP + 64 * h, sv, dv);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float dd[2];
+  for (int cc = 0; cc < 2; ++cc) {
+    const int c = 2 * h + cc;
+    uint32_t w[16];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int k = 2 * i + e;
-      const float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -lse2));
-      float dsv = pv * (__uint_as_float(dv[k]) - dl);
-      if (MASK) {
-        const int col = c * 32 + k;
-        if (!(col >= lo && col <= hi)) dsv = 0.f;
+    for (int i = 0; i < 16; ++i) {
+      float dd[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int k = cc * 32 + 2 * i + e;
+        const float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -lse2));
+        float dsv = pv * (__uint_as_float(dv[k]) - dl);
+        if (MASK) {
+          const int col = c * 32 + 2 * i + e;
+          if (!(col >= lo && col <= hi)) dsv = 0.f;
+        }
+        dd[e] = dsv;
       }
-      dd[e] = dsv;
+      w[i] = tc::pack_bf16(dd[0], dd[1]);
     }
-    w[i] = tc::pack_bf16(dd[0], dd[1]);
+    tc::tmem_st_x16(tS + c * 32, w);
   }
-  tc::tmem_st_x16(tS + c * 32, w);
 }
 
 // Store 32 fp32 values (times f) of one row as bf16 to global.
@@ -334,11 +356,18 @@ __global__ void __launch_bounds__(384, 1)
       tc::prefetch_tmap(&tmQ);
       tc::prefetch_tmap(&tmdO);
       const int G = p.G;
-      produce<D>(smem, bars, abort, &tmK, jk * D, &tmV, jk * D, (int)u0, g, &tmQ, &tmdO, n_it,
-                 [&](int it, int, int& c0, int& c1) {
-                   c0 = (jk * G + it % G) * D;
-                   c1 = (int)(tq0 + (int64_t)(it / G) * BT);
-                 });
+      produce<D, true>(
+          smem, bars, abort, &tmK, jk * D, &tmV, jk * D, (int)u0, g, &tmQ, &tmdO, n_it,
+          [&](int it, int, int& c0, int& c1) {
+            c0 = (jk * G + it % G) * D;
+            c1 = (int)(tq0 + (int64_t)(it / G) * BT);
+          },
+          [&](int it, int w) -> const float* {
+            // lse2 next to the Q tile, delta next to the dO tile
+            const int64_t off = ((int64_t)g * p.hq + jk * G + it % G) * p.S_ws + tq0 +
+                                (int64_t)(it / G) * BT;
+            return (w == 0 ? p.lse2 : p.delta) + off;
+          });
     }
   } else if (warp == 1) {
     if (lane == 0 && n_it > 0) mma_loop<D, true>(smem, bars, abort, tmem, n_it);
@@ -353,30 +382,29 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int64_t t0 = tq0 + (int64_t)(it / p.G) * BT;
-      const int jq = jk * p.G + it % p.G;
-      // per-query LSE*log2(e) and delta of this tile: rows of S_ws (a
-      // multiple of BT) entries, so these 16-byte loads are aligned and the
-      // last tile's columns past S_pad read the filled pad entries
-      const float* lse2 = p.lse2 + ((int64_t)g * p.hq + jq) * p.S_ws + t0;
-      const float* dl = p.delta + ((int64_t)g * p.hq + jq) * p.S_ws + t0;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->s_full, it & 1, abort) &&
-                                       tc::mbar_wait(&bars->dp_full, it & 1, abort));
+      const int s0 = (2 * it) % C::NSTAGE, s1 = (2 * it + 1) % C::NSTAGE;
+      ok = __all_sync(0xffffffffu,
+                      tc::mbar_wait(&bars->sd_full[half], it & 1, abort) &&
+                          tc::mbar_wait(&bars->ring_full[s0], ((2 * it) / C::NSTAGE) & 1, abort) &&
+                          tc::mbar_wait(&bars->ring_full[s1], ((2 * it + 1) / C::NSTAGE) & 1, abort));
       if (!ok) break;
       tc::fence_after_sync();
+      // per-query LSE*log2(e) and delta of this tile, staged by the producer
+      const float* lse2 = reinterpret_cast<const float*>(smem + C::VEC_OFF + s0 * BT * 4);
+      const float* dl = reinterpret_cast<const float*>(smem + C::VEC_OFF + s1 * BT * 4);
       const int lo = (int)max((int64_t)0, min((int64_t)BT, u - t0));
       const int hi = de < 0 ? -1 : (int)min((int64_t)BT - 1, de - 1 - t0);
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        if (mask) dkdv_chunk<true>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
-        else dkdv_chunk<false>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
-      }
+      if (mask) dkdv_half<true>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
+      else dkdv_half<false>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bars->p_full);
+      tc::mbar_arrive(&bars->p_full[half]);
     }
     if (ok && n_it > 0) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->mma_done, (n_it - 1) & 1, abort));
+      const uint32_t ph = (n_it - 1) & 1;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], ph, abort) &&
+                                       tc::mbar_wait(&bars->done[1], ph, abort));
       tc::fence_after_sync();
     }
     // epilogue: the left half writes dV, the right half dK
@@ -449,11 +477,13 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0 && n_kv > 0) {
       tc::prefetch_tmap(&tmK);
       tc::prefetch_tmap(&tmV);
-      produce<D>(smem, bars, abort, &tmQ, jq * D, &tmdO, jq * D, (int)t0, g, &tmK, &tmV, n_kv,
-                 [&](int it, int, int& c0, int& c1) {
-                   c0 = jk * D;
-                   c1 = (int)(kv_start + (int64_t)it * BT);
-                 });
+      produce<D, false>(
+          smem, bars, abort, &tmQ, jq * D, &tmdO, jq * D, (int)t0, g, &tmK, &tmV, n_kv,
+          [&](int it, int, int& c0, int& c1) {
+            c0 = jk * D;
+            c1 = (int)(kv_start + (int64_t)it * BT);
+          },
+          [&](int, int) -> const float* { return nullptr; });
     }
   } else if (warp == 1) {
     if (lane == 0 && n_kv > 0) mma_loop<D, false>(smem, bars, abort, tmem, n_kv);
@@ -473,25 +503,23 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
     bool ok = true;
     for (int it = 0; it < n_kv; ++it) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->s_full, it & 1, abort) &&
-                                       tc::mbar_wait(&bars->dp_full, it & 1, abort));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full[half], it & 1, abort));
       if (!ok) break;
       tc::fence_after_sync();
       const int64_t u0 = kv_start + (int64_t)it * BT;
       const int lo = (int)max((int64_t)0, min((int64_t)BT, ds - u0));
       const int hi = ds < 0 ? -1 : (int)min((int64_t)BT - 1, t - u0);
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        if (mask) dq_chunk<true>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
-        else dq_chunk<false>(tS, tP, 2 * half + cc, lo, hi, lse2, dl, p.scale_log2);
-      }
+      if (mask) dq_half<true>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
+      else dq_half<false>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bars->p_full);
+      tc::mbar_arrive(&bars->p_full[half]);
     }
     if (ok && n_kv > 0) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->mma_done, (n_kv - 1) & 1, abort));
+      const uint32_t ph = (n_kv - 1) & 1;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], ph, abort) &&
+                                       tc::mbar_wait(&bars->done[1], ph, abort));
       tc::fence_after_sync();
     }
     const bool have = ok && n_kv > 0;

@@ -82,56 +82,38 @@ __device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
   return p.cu ? (int64_t)__ldg(p.cu + d) : 0;
 }
 
-// Row max of this thread's S row (128 fp32 columns in TMEM).  With MASK the
-// columns outside [lo, hi] count as -inf; without it no column is tested.
-template <bool MASK>
-__device__ __forceinline__ float s_row_max(uint32_t tS, int lo, int hi) {
+// One softmax step on this thread's S row: the 128 fp32 columns are read
+// from TMEM with a single load, masked (MASK: columns outside [lo, hi] are
+// -inf), reduced to the row max, and after `rescale_fn` picked the running
+// max m_eff, turned into P = exp2(S*sl2 - m_eff) written as bf16 pairs over
+// the first 64 columns.  Returns the fp32 row sum.
+template <bool MASK, typename MaxFn>
+__device__ __forceinline__ float softmax_row(uint32_t tS, int lo, int hi, float sl2,
+                                             MaxFn rescale_fn) {
+  uint32_t v[128];
+  tc::tmem_ld_x128(tS, v);
+  if (MASK) {
+#pragma unroll
+    for (int col = 0; col < 128; ++col)
+      if (!(col >= lo && col <= hi)) v[col] = __float_as_uint(-INFINITY);
+  }
   float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < BN / 32; ++c) {
-    uint32_t v[32];
-    tc::tmem_ld_x32(tS + c * 32, v);
-#pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        x[e] = __uint_as_float(v[i + e]);
-        if (MASK) {
-          const int col = c * 32 + i + e;
-          if (!(col >= lo && col <= hi)) x[e] = -INFINITY;
-        }
-      }
-      m0 = tc::max3(m0, x[0], x[1]);
-      m1 = tc::max3(m1, x[2], x[3]);
-      m2 = tc::max3(m2, x[4], x[5]);
-      m3 = tc::max3(m3, x[6], x[7]);
-    }
+  for (int i = 0; i < 128; i += 8) {
+    m0 = tc::max3(m0, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+    m1 = tc::max3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+    m2 = tc::max3(m2, __uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+    m3 = tc::max3(m3, __uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
   }
-  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-}
-
-// P = exp2(S*scale_log2 - m_eff) written as bf16 pairs over the first 64
-// columns of the S row; returns the fp32 row sum.
-template <bool MASK>
-__device__ __forceinline__ float s_row_exp(uint32_t tS, int lo, int hi, float sl2, float m_eff) {
+  const float m_eff = rescale_fn(fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)));
   float r0 = 0.f, r1 = 0.f;
 #pragma unroll
   for (int c = 0; c < BN / 32; ++c) {
-    uint32_t v[32];
-    tc::tmem_ld_x32(tS + c * 32, v);
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      float x0 = __uint_as_float(v[2 * i]);
-      float x1 = __uint_as_float(v[2 * i + 1]);
-      if (MASK) {
-        const int col = c * 32 + 2 * i;
-        if (!(col >= lo && col <= hi)) x0 = -INFINITY;
-        if (!(col + 1 >= lo && col + 1 <= hi)) x1 = -INFINITY;
-      }
-      const float p0 = tc::ex2(fmaf(x0, sl2, -m_eff));
-      const float p1 = tc::ex2(fmaf(x1, sl2, -m_eff));
+      const float p0 = tc::ex2(fmaf(__uint_as_float(v[c * 32 + 2 * i]), sl2, -m_eff));
+      const float p1 = tc::ex2(fmaf(__uint_as_float(v[c * 32 + 2 * i + 1]), sl2, -m_eff));
       r0 += p0;
       r1 += p1;
       w[i] = tc::pack_bf16(p0, p1);
@@ -309,18 +291,19 @@ __global__ void __launch_bounds__(384, 1)
         // keys u0+c visible to row t iff ds <= u0+c <= t  (c in [lo, hi])
         const int lo = (int)max((int64_t)0, min((int64_t)BN, ds - u0));
         const int hi = ds < 0 ? -1 : (int)min((int64_t)BN - 1, t - u0);
-        // pass 1: row max; the mask is warp-uniform, so fully visible tiles
-        // take the path without per-column tests
-        const float mx = mask ? s_row_max<true>(tS, lo, hi) : s_row_max<false>(tS, lo, hi);
-        const float m_tile = mx * p.scale_log2;
-        const float m_new = fmaxf(m, m_tile);
-        const bool rescale = m_new > m + kRescaleThreshold;
-        const float m_use = rescale ? m_new : m;
-        const float alpha = rescale ? tc::ex2(m - m_new) : 1.f;
-        const float m_eff = m_use == -INFINITY ? 0.f : m_use;
-        // pass 2: P = exp2(S*scale*log2e - m), written as bf16 over S
-        const float rowsum = mask ? s_row_exp<true>(tS, lo, hi, p.scale_log2, m_eff)
-                                  : s_row_exp<false>(tS, lo, hi, p.scale_log2, m_eff);
+        // the mask is warp-uniform, so fully visible tiles take the path
+        // without per-column tests
+        bool rescale = false;
+        float alpha = 1.f, m_use = m;
+        auto pick = [&](float mx) {
+          const float m_new = fmaxf(m, mx * p.scale_log2);
+          rescale = m_new > m + kRescaleThreshold;
+          m_use = rescale ? m_new : m;
+          alpha = rescale ? tc::ex2(m - m_new) : 1.f;
+          return m_use == -INFINITY ? 0.f : m_use;
+        };
+        const float rowsum = mask ? softmax_row<true>(tS, lo, hi, p.scale_log2, pick)
+                                  : softmax_row<false>(tS, lo, hi, p.scale_log2, pick);
         l = l * alpha + rowsum;
         m = m_use;
         if (jt > 0 && __any_sync(0xffffffffu, rescale)) {
