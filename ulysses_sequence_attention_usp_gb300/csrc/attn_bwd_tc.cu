@@ -50,16 +50,16 @@ struct Cfg {
   static constexpr int SMEM = VEC_OFF + NSTAGE * BT * 4 + 1024;
 };
 
-// Each 128-column tile is processed as two 64-column halves with their own
-// TMEM regions and barriers, so the MMAs of one half run while the
-// elementwise warps work on the other.
 struct Bars {
   uint64_t fix_full;
   uint64_t ring_full[8];
   uint64_t ring_empty[8];
-  uint64_t sd_full[2];    // S and dP of half h computed
-  uint64_t p_full[2];     // elementwise of half h published (128 arrivals)
-  uint64_t done[2];       // accumulation MMAs of half h completed
+  uint64_t sd_full;       // S and dP (or S^T and dP^T) of the iteration computed
+  uint64_t consumed;      // dq: both elementwise groups read S and dP (256 arrivals)
+  uint64_t p_full[2];     // dkdv: P^T/dS^T published ([0], 256 arrivals);
+                          // dq: dS written to buffer b ([b], 256 arrivals)
+  uint64_t done[2];       // dkdv: accumulation MMAs done ([0]); dq: dQ MMA that
+                          // read dS buffer b done ([b])
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -100,10 +100,11 @@ __device__ __forceinline__ void init_common(Bars* bars) {
     tc::mbar_init(&bars->ring_full[s], 1);
     tc::mbar_init(&bars->ring_empty[s], 1);
   }
-  for (int h = 0; h < 2; ++h) {
-    tc::mbar_init(&bars->sd_full[h], 1);
-    tc::mbar_init(&bars->p_full[h], 128);
-    tc::mbar_init(&bars->done[h], 1);
+  tc::mbar_init(&bars->sd_full, 1);
+  tc::mbar_init(&bars->consumed, 256);
+  for (int b = 0; b < 2; ++b) {
+    tc::mbar_init(&bars->p_full[b], 256);
+    tc::mbar_init(&bars->done[b], 1);
   }
   tc::mbar_init(&bars->drain, 1);
   bars->abort = 0;
@@ -152,22 +153,31 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int*
   }
 }
 
-// MMA issuer shared by both kernels.  Iteration `it` streams ring tiles R0
-// and R1 against the stationary tiles F0 and F1.  For each half h (rows
-// [64h, 64h+64) of the ring tiles, TMEM columns [64h, 64h+64) of T0/T1):
-//   T0_h = F0 R0_h^T, T1_h = F1 R1_h^T          (SS, M=128 N=64 K=D)
-// and, once the elementwise warps of half h published E0_h (over T0_h) and
-// E1_h (over T1_h), the accumulation over that half's 64 rows (K=64):
-//   dkdv:  A0 += E0_h R1_h (dV += P^T dO),  A1 += E1_h R0_h (dK += dS^T Q)
-//   dq:    A0 += E0_h R0_h (dQ += dS K)
-// T0_h/T1_h are rewritten for iteration it+1 only after done[h] of
-// iteration it, i.e. after the accumulation MMAs that read E0_h/E1_h.
-template <int D, bool DKDV>
-__device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int* abort,
-                                         uint32_t tmem, int n_it) {
+// Issue T = F x R^T for one 128x128 tile pair (SS, K-major operands, K = D):
+// F is a stationary tile, R a ring tile.
+template <int D>
+__device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint32_t f, uint32_t r) {
+  using C = Cfg<D>;
+  constexpr uint32_t id = tc::idesc_bf16(128, BT, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
+    tc::mma_ss(d_tmem, tc::desc_sw128(f + off, 16, 1024), tc::desc_sw128(r + off, 16, 1024), id,
+               kk > 0);
+  }
+}
+
+// dK/dV MMA issuer.  Iteration `it` streams ring tiles Q (R0) and dO (R1):
+//   S^T = K Q^T (T0),  dP^T = V dO^T (T1)                (SS)
+// then, once both elementwise groups published P^T over T0 and dS^T over T1
+// (bf16, first 16 columns of every 32-column chunk):
+//   dV += P^T dO,  dK += dS^T Q                          (TS, K = 128)
+// T0/T1 are rewritten for iteration it+1 only after those MMAs completed.
+template <int D>
+__device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatile int* abort,
+                                              uint32_t tmem, int n_it) {
   using C = Cfg<D>;
   constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, A1 = 256 + D;
-  constexpr uint32_t id_st = tc::idesc_bf16(128, BT / 2, false);
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
@@ -177,45 +187,77 @@ __device__ __forceinline__ void mma_loop(uint8_t* smem, Bars* bars, volatile int
     const int s1 = (2 * it + 1) % C::NSTAGE, u1 = (2 * it + 1) / C::NSTAGE;
     if (!(ok = tc::mbar_wait(&bars->ring_full[s0], u0 & 1, abort))) break;
     if (!(ok = tc::mbar_wait(&bars->ring_full[s1], u1 & 1, abort))) break;
-    for (int h = 0; h < 2 && ok; ++h) {
-      if (it > 0 && !(ok = tc::mbar_wait(&bars->done[h], (it - 1) & 1, abort))) break;
-      tc::fence_after_sync();
-      const uint32_t rows = h * 64 * 128;     // byte offset of row 64h in a box
+    if (it > 0 && !(ok = tc::mbar_wait(&bars->done[0], (it - 1) & 1, abort))) break;
+    tc::fence_after_sync();
+    mma_tile_ss<D>(tmem + T0, fix, ring + s0 * C::TILE);
+    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + s1 * C::TILE);
+    tc::mma_commit(&bars->sd_full);
+    if (!(ok = tc::mbar_wait(&bars->p_full[0], it & 1, abort))) break;
+    tc::fence_after_sync();
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
-        tc::mma_ss(tmem + T0 + 64 * h, tc::desc_sw128(fix + off, 16, 1024),
-                   tc::desc_sw128(ring + s0 * C::TILE + off + rows, 16, 1024), id_st, kk > 0);
-      }
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
-        tc::mma_ss(tmem + T1 + 64 * h, tc::desc_sw128(fix + C::TILE + off, 16, 1024),
-                   tc::desc_sw128(ring + s1 * C::TILE + off + rows, 16, 1024), id_st, kk > 0);
-      }
-      tc::mma_commit(&bars->sd_full[h]);
+    for (int kk = 0; kk < BT / 16; ++kk) {
+      const uint32_t ka = 32 * (kk >> 1) + 8 * (kk & 1);
+      const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+      tc::mma_ts(tmem + A0, tmem + T0 + ka,
+                 tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
+      tc::mma_ts(tmem + A1, tmem + T1 + ka,
+                 tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
     }
-    for (int h = 0; h < 2 && ok; ++h) {
-      if (!(ok = tc::mbar_wait(&bars->p_full[h], it & 1, abort))) break;
+    tc::mma_commit(&bars->done[0]);
+    tc::mma_commit(&bars->ring_empty[s0]);
+    tc::mma_commit(&bars->ring_empty[s1]);
+  }
+  if (!ok) {
+    tc::mma_commit(&bars->drain);
+    tc::mbar_wait(&bars->drain, 0, nullptr, 100000000ull);
+  }
+}
+
+// dQ MMA issuer.  Iteration j streams key tile K_j (R0) and V_j (R1):
+//   S(j) = Q K_j^T (T0),  dP(j) = dO V_j^T (T1)          (SS)
+//   dQ += dS(j) K_j   with dS(j) in TMEM buffer j%2       (TS, K = 128)
+// S(j+1) and dP(j+1) are issued as soon as the elementwise groups have read
+// S(j) and dP(j) ("consumed"), before they finish dS(j), so the tensor pipe
+// keeps working while they compute.  Buffer b of dS is rewritten for j+2
+// only after done[b] (the dQ MMA that read it).
+template <int D>
+__device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile int* abort,
+                                            uint32_t tmem, int n_it) {
+  using C = Cfg<D>;
+  constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, R = 384;
+  constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
+  const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
+  const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
+  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort) &&
+            tc::mbar_wait(&bars->ring_full[0], 0, abort) &&
+            tc::mbar_wait(&bars->ring_full[1], 0, abort);
+  if (ok) {
+    tc::fence_after_sync();
+    mma_tile_ss<D>(tmem + T0, fix, ring);
+    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + C::TILE);
+    tc::mma_commit(&bars->sd_full);
+  }
+  for (int j = 0; ok && j < n_it; ++j) {
+    const int s0 = (2 * j) % C::NSTAGE, s1 = (2 * j + 1) % C::NSTAGE;
+    if (!(ok = tc::mbar_wait(&bars->consumed, j & 1, abort))) break;
+    if (j + 1 < n_it) {
+      const int n0 = (2 * j + 2) % C::NSTAGE, n1 = (2 * j + 3) % C::NSTAGE;
+      if (!(ok = tc::mbar_wait(&bars->ring_full[n0], ((2 * j + 2) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait(&bars->ring_full[n1], ((2 * j + 3) / C::NSTAGE) & 1, abort))) break;
       tc::fence_after_sync();
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const int kk = 4 * h + k4;             // 16-row K step within the tile
-        const uint32_t ka = 32 * (kk >> 1) + 8 * (kk & 1);
-        const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-        if (DKDV) {
-          tc::mma_ts(tmem + A0, tmem + T0 + ka,
-                     tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
-          tc::mma_ts(tmem + A1, tmem + T1 + ka,
-                     tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
-        } else {
-          tc::mma_ts(tmem + A0, tmem + T0 + ka,
-                     tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
-        }
-      }
-      tc::mma_commit(&bars->done[h]);
+      mma_tile_ss<D>(tmem + T0, fix, ring + n0 * C::TILE);
+      mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
+      tc::mma_commit(&bars->sd_full);
     }
-    if (!ok) break;
+    const int b = j & 1;
+    if (!(ok = tc::mbar_wait(&bars->p_full[b], (j >> 1) & 1, abort))) break;
+    tc::fence_after_sync();
+#pragma unroll
+    for (int kk = 0; kk < BT / 16; ++kk)
+      tc::mma_ts(tmem + A0, tmem + R + 64 * b + 8 * kk,
+                 tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+    tc::mma_commit(&bars->done[b]);
     tc::mma_commit(&bars->ring_empty[s0]);
     tc::mma_commit(&bars->ring_empty[s1]);
   }
@@ -268,36 +310,42 @@ __device__ __forceinline__ void dkdv_half(uint32_t tS, uint32_t tP, int h, int l
   }
 }
 
-// dQ elementwise work on half h of this thread's query row:
-// dS = exp2(S*sl2 - lse2) (dP - delta), bf16 over the first 16 columns of
-// each 32-column chunk.
+// dQ elementwise work on half h (keys [64h, 64h+64)) of this thread's query
+// row: read S and dP, let the MMA issuer reuse them ("consumed"), compute
+// dS = exp2(S*sl2 - lse2) (dP - delta) and, once dS buffer `b` is free,
+// write it there as bf16 (32 columns: K steps 4h..4h+3).
 template <bool MASK>
-__device__ __forceinline__ void dq_half(uint32_t tS, uint32_t tP, int h, int lo, int hi,
-                                        float lse2, float dl, float sl2) {
+__device__ __forceinline__ bool dq_half(uint32_t tS, uint32_t tP, uint32_t tR, int h, int lo,
+                                        int hi, float lse2, float dl, float sl2, Bars* bars,
+                                        int j, volatile int* abort) {
   uint32_t sv[64], dv[64];
   tc::tmem_ld2_x64(tS + 64 * h, tP + 64 * h, sv, dv);
+  tc::fence_before_sync();
+  tc::mbar_arrive(&bars->consumed);
+  uint32_t w[32];
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
-    const int c = 2 * h + cc;
-    uint32_t w[16];
+  for (int i = 0; i < 32; ++i) {
+    float dd[2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float dd[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int k = cc * 32 + 2 * i + e;
-        const float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -lse2));
-        float dsv = pv * (__uint_as_float(dv[k]) - dl);
-        if (MASK) {
-          const int col = c * 32 + 2 * i + e;
-          if (!(col >= lo && col <= hi)) dsv = 0.f;
-        }
-        dd[e] = dsv;
+    for (int e = 0; e < 2; ++e) {
+      const int k = 2 * i + e;
+      const float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -lse2));
+      float dsv = pv * (__uint_as_float(dv[k]) - dl);
+      if (MASK) {
+        const int col = 64 * h + k;
+        if (!(col >= lo && col <= hi)) dsv = 0.f;
       }
-      w[i] = tc::pack_bf16(dd[0], dd[1]);
+      dd[e] = dsv;
     }
-    tc::tmem_st_x16(tS + c * 32, w);
+    w[i] = tc::pack_bf16(dd[0], dd[1]);
   }
+  if (j >= 2) {   // the dQ MMA of iteration j-2 read this buffer
+    if (!__all_sync(0xffffffffu, tc::mbar_wait(&bars->done[j & 1], ((j >> 1) - 1) & 1, abort)))
+      return false;
+    tc::fence_after_sync();
+  }
+  tc::tmem_st_x32(tR + 32 * h, w);
+  return true;
 }
 
 // Store 32 fp32 values (times f) of one row as bf16 to global.
@@ -370,7 +418,7 @@ __global__ void __launch_bounds__(384, 1)
           });
     }
   } else if (warp == 1) {
-    if (lane == 0 && n_it > 0) mma_loop<D, true>(smem, bars, abort, tmem, n_it);
+    if (lane == 0 && n_it > 0) mma_loop_dkdv<D>(smem, bars, abort, tmem, n_it);
   } else if (warp >= 4) {
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)
@@ -384,7 +432,7 @@ __global__ void __launch_bounds__(384, 1)
       const int64_t t0 = tq0 + (int64_t)(it / p.G) * BT;
       const int s0 = (2 * it) % C::NSTAGE, s1 = (2 * it + 1) % C::NSTAGE;
       ok = __all_sync(0xffffffffu,
-                      tc::mbar_wait(&bars->sd_full[half], it & 1, abort) &&
+                      tc::mbar_wait(&bars->sd_full, it & 1, abort) &&
                           tc::mbar_wait(&bars->ring_full[s0], ((2 * it) / C::NSTAGE) & 1, abort) &&
                           tc::mbar_wait(&bars->ring_full[s1], ((2 * it + 1) / C::NSTAGE) & 1, abort));
       if (!ok) break;
@@ -399,12 +447,10 @@ __global__ void __launch_bounds__(384, 1)
       else dkdv_half<false>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bars->p_full[half]);
+      tc::mbar_arrive(&bars->p_full[0]);
     }
     if (ok && n_it > 0) {
-      const uint32_t ph = (n_it - 1) & 1;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], ph, abort) &&
-                                       tc::mbar_wait(&bars->done[1], ph, abort));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], (n_it - 1) & 1, abort));
       tc::fence_after_sync();
     }
     // epilogue: the left half writes dV, the right half dK
@@ -486,7 +532,7 @@ __global__ void __launch_bounds__(384, 1)
           [&](int, int) -> const float* { return nullptr; });
     }
   } else if (warp == 1) {
-    if (lane == 0 && n_kv > 0) mma_loop<D, false>(smem, bars, abort, tmem, n_kv);
+    if (lane == 0 && n_kv > 0) mma_loop_dq<D>(smem, bars, abort, tmem, n_kv);
   } else if (warp >= 4) {
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)
@@ -502,24 +548,26 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
     const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
     bool ok = true;
+    const uint32_t tR = tc::tmem_addr(tmem, quarter * 32, 384);
     for (int it = 0; it < n_kv; ++it) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full[half], it & 1, abort));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full, it & 1, abort));
       if (!ok) break;
       tc::fence_after_sync();
       const int64_t u0 = kv_start + (int64_t)it * BT;
       const int lo = (int)max((int64_t)0, min((int64_t)BT, ds - u0));
       const int hi = ds < 0 ? -1 : (int)min((int64_t)BT - 1, t - u0);
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
-      if (mask) dq_half<true>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
-      else dq_half<false>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
+      const uint32_t tRb = tR + 64 * (it & 1);
+      ok = mask ? dq_half<true>(tS, tP, tRb, half, lo, hi, lse2, dl, p.scale_log2, bars, it, abort)
+                : dq_half<false>(tS, tP, tRb, half, lo, hi, lse2, dl, p.scale_log2, bars, it, abort);
+      if (!ok) break;
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bars->p_full[half]);
+      tc::mbar_arrive(&bars->p_full[it & 1]);
     }
     if (ok && n_kv > 0) {
-      const uint32_t ph = (n_kv - 1) & 1;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], ph, abort) &&
-                                       tc::mbar_wait(&bars->done[1], ph, abort));
+      const int jl = n_kv - 1;   // the last dQ MMA completes after all earlier ones
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[jl & 1], (jl >> 1) & 1, abort));
       tc::fence_after_sync();
     }
     const bool have = ok && n_kv > 0;
