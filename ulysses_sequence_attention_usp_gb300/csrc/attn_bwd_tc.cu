@@ -54,12 +54,13 @@ struct Bars {
   uint64_t fix_full;
   uint64_t ring_full[8];
   uint64_t ring_empty[8];
-  uint64_t sd_full;       // S and dP (or S^T and dP^T) of the iteration computed
+  uint64_t sd_full;       // dq: S and dP of the iteration computed; dkdv: S^T computed
+  uint64_t dp_full;       // dkdv: dP^T computed
   uint64_t consumed;      // dq: both elementwise groups read S and dP (256 arrivals)
-  uint64_t p_full[2];     // dkdv: P^T/dS^T published ([0], 256 arrivals);
-                          // dq: dS written to buffer b ([b], 256 arrivals)
-  uint64_t done[2];       // dkdv: accumulation MMAs done ([0]); dq: dQ MMA that
-                          // read dS buffer b done ([b])
+  uint64_t p_full[2];     // dkdv: P^T published ([0]), dS^T published ([1]);
+                          // dq: dS written to buffer b ([b]); 256 arrivals each
+  uint64_t done[2];       // dkdv: dV MMA done ([0]), dK MMA done ([1]);
+                          // dq: dQ MMA that read dS buffer b done ([b])
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -101,6 +102,7 @@ __device__ __forceinline__ void init_common(Bars* bars) {
     tc::mbar_init(&bars->ring_empty[s], 1);
   }
   tc::mbar_init(&bars->sd_full, 1);
+  tc::mbar_init(&bars->dp_full, 1);
   tc::mbar_init(&bars->consumed, 256);
   for (int b = 0; b < 2; ++b) {
     tc::mbar_init(&bars->p_full[b], 256);
@@ -168,11 +170,13 @@ __device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint32_t f, uint32_
 }
 
 // dK/dV MMA issuer.  Iteration `it` streams ring tiles Q (R0) and dO (R1):
-//   S^T = K Q^T (T0),  dP^T = V dO^T (T1)                (SS)
-// then, once both elementwise groups published P^T over T0 and dS^T over T1
-// (bf16, first 16 columns of every 32-column chunk):
-//   dV += P^T dO,  dK += dS^T Q                          (TS, K = 128)
-// T0/T1 are rewritten for iteration it+1 only after those MMAs completed.
+//   S^T = K Q^T (T0) -> sd_full,   dP^T = V dO^T (T1) -> dp_full     (SS)
+//   dV += P^T dO  once P^T is published over T0                     (TS)
+//   dK += dS^T Q  once dS^T is published over T1                    (TS)
+// The elementwise groups compute P^T while dP^T is still in the tensor
+// pipe and dS^T while dV runs.  S^T of the next iteration is issued once dV
+// has read P^T (done[0]), dP^T once dK has read dS^T (done[1]); both are
+// then queued behind the MMA still running.
 template <int D>
 __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatile int* abort,
                                               uint32_t tmem, int n_it) {
@@ -190,20 +194,27 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
     if (it > 0 && !(ok = tc::mbar_wait(&bars->done[0], (it - 1) & 1, abort))) break;
     tc::fence_after_sync();
     mma_tile_ss<D>(tmem + T0, fix, ring + s0 * C::TILE);
-    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + s1 * C::TILE);
     tc::mma_commit(&bars->sd_full);
+    if (it > 0 && !(ok = tc::mbar_wait(&bars->done[1], (it - 1) & 1, abort))) break;
+    tc::fence_after_sync();
+    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + s1 * C::TILE);
+    tc::mma_commit(&bars->dp_full);
     if (!(ok = tc::mbar_wait(&bars->p_full[0], it & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
-    for (int kk = 0; kk < BT / 16; ++kk) {
-      const uint32_t ka = 32 * (kk >> 1) + 8 * (kk & 1);
-      const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-      tc::mma_ts(tmem + A0, tmem + T0 + ka,
-                 tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
-      tc::mma_ts(tmem + A1, tmem + T1 + ka,
-                 tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc, acc);
-    }
+    for (int kk = 0; kk < BT / 16; ++kk)
+      tc::mma_ts(tmem + A0, tmem + T0 + 32 * (kk >> 1) + 8 * (kk & 1),
+                 tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
     tc::mma_commit(&bars->done[0]);
+    if (!(ok = tc::mbar_wait(&bars->p_full[1], it & 1, abort))) break;
+    tc::fence_after_sync();
+#pragma unroll
+    for (int kk = 0; kk < BT / 16; ++kk)
+      tc::mma_ts(tmem + A1, tmem + T1 + 32 * (kk >> 1) + 8 * (kk & 1),
+                 tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+    tc::mma_commit(&bars->done[1]);
     tc::mma_commit(&bars->ring_empty[s0]);
     tc::mma_commit(&bars->ring_empty[s1]);
   }
@@ -267,46 +278,62 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
   }
 }
 
-// dK/dV elementwise work on half h (columns [64h, 64h+64)) of this thread's
-// key row, read from TMEM with one wait:
-//   P^T = exp2(S^T*sl2 - lse2[col]),  dS^T = P^T (dP^T - delta[col]),
-// both written as bf16 over the first 16 columns of each 32-column chunk.
+// dK/dV elementwise work on half h (queries [64h, 64h+64)) of this thread's
+// key row, in two phases so that each overlaps an MMA:
+//   phase 1 (while dP^T is computed): P^T = exp2(S^T*sl2 - lse2[col]),
+//            written as bf16 over S^T, kept in fp32 registers;
+//   phase 2 (while dV is computed):   dS^T = P^T (dP^T - delta[col]),
+//            written as bf16 over dP^T.
+// bf16 values of each 32-column chunk go to that chunk's first 16 columns.
 // Columns outside [lo, hi] are zero when MASK.
 template <bool MASK>
-__device__ __forceinline__ void dkdv_half(uint32_t tS, uint32_t tP, int h, int lo, int hi,
-                                          const float* lse2, const float* dl, float sl2) {
-  uint32_t sv[64], dv[64];
-  tc::tmem_ld2_x64(tS + 64 * h, tP + 64 * h, sv, dv);
+__device__ __forceinline__ void dkdv_phase_p(uint32_t tS, int h, int lo, int hi,
+                                             const float* lse2, float sl2, float (&pf)[64]) {
+  uint32_t sv[64];
+  tc::tmem_ld_x64(tS + 64 * h, sv);
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
-    const int c = 2 * h + cc;
-    uint32_t pw[16], dw[16];
+    uint32_t pw[16];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {   // shared memory, same address in every lane
-      const float4 a = reinterpret_cast<const float4*>(lse2 + c * 32)[i];
-      const float4 b = reinterpret_cast<const float4*>(dl + c * 32)[i];
+      const float4 a = reinterpret_cast<const float4*>(lse2 + 64 * h + 32 * cc)[i];
       const float l2[4] = {a.x, a.y, a.z, a.w};
-      const float d2[4] = {b.x, b.y, b.z, b.w};
-      float pp[4], dd[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int k = cc * 32 + 4 * i + e;
+        const int k = 32 * cc + 4 * i + e;
         float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -l2[e]));
-        float dsv = pv * (__uint_as_float(dv[k]) - d2[e]);
         if (MASK) {
-          const int col = c * 32 + 4 * i + e;
-          if (!(col >= lo && col <= hi)) { pv = 0.f; dsv = 0.f; }
+          const int col = 64 * h + k;
+          if (!(col >= lo && col <= hi)) pv = 0.f;
         }
-        pp[e] = pv;
-        dd[e] = dsv;
+        pf[k] = pv;
       }
-      pw[2 * i] = tc::pack_bf16(pp[0], pp[1]);
-      pw[2 * i + 1] = tc::pack_bf16(pp[2], pp[3]);
+      pw[2 * i] = tc::pack_bf16(pf[32 * cc + 4 * i], pf[32 * cc + 4 * i + 1]);
+      pw[2 * i + 1] = tc::pack_bf16(pf[32 * cc + 4 * i + 2], pf[32 * cc + 4 * i + 3]);
+    }
+    tc::tmem_st_x16(tS + 64 * h + 32 * cc, pw);
+  }
+}
+
+__device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, int h, const float* dl,
+                                              const float (&pf)[64]) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    uint32_t dv[32];
+    tc::tmem_ld_x32(tP + 64 * h + 32 * cc, dv);
+    uint32_t dw[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 b = reinterpret_cast<const float4*>(dl + 64 * h + 32 * cc)[i];
+      const float d2[4] = {b.x, b.y, b.z, b.w};
+      float dd[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        dd[e] = pf[32 * cc + 4 * i + e] * (__uint_as_float(dv[4 * i + e]) - d2[e]);
       dw[2 * i] = tc::pack_bf16(dd[0], dd[1]);
       dw[2 * i + 1] = tc::pack_bf16(dd[2], dd[3]);
     }
-    tc::tmem_st_x16(tS + c * 32, pw);
-    tc::tmem_st_x16(tP + c * 32, dw);
+    tc::tmem_st_x16(tP + 64 * h + 32 * cc, dw);
   }
 }
 
@@ -443,14 +470,22 @@ __global__ void __launch_bounds__(384, 1)
       const int lo = (int)max((int64_t)0, min((int64_t)BT, u - t0));
       const int hi = de < 0 ? -1 : (int)min((int64_t)BT - 1, de - 1 - t0);
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
-      if (mask) dkdv_half<true>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
-      else dkdv_half<false>(tS, tP, half, lo, hi, lse2, dl, p.scale_log2);
+      float pf[64];
+      if (mask) dkdv_phase_p<true>(tS, half, lo, hi, lse2, p.scale_log2, pf);
+      else dkdv_phase_p<false>(tS, half, lo, hi, lse2, p.scale_log2, pf);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bars->p_full[0]);
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->dp_full, it & 1, abort));
+      if (!ok) break;
+      tc::fence_after_sync();
+      dkdv_phase_ds(tP, half, dl, pf);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->p_full[1]);
     }
-    if (ok && n_it > 0) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], (n_it - 1) & 1, abort));
+    if (ok && n_it > 0) {   // dK is the last MMA; it completes after dV
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[1], (n_it - 1) & 1, abort));
       tc::fence_after_sync();
     }
     // epilogue: the left half writes dV, the right half dK
