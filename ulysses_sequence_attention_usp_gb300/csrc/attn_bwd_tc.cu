@@ -173,10 +173,11 @@ __device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint32_t f, uint32_
 //   S^T = K Q^T (T0) -> sd_full,   dP^T = V dO^T (T1) -> dp_full     (SS)
 //   dV += P^T dO  once P^T is published over T0                     (TS)
 //   dK += dS^T Q  once dS^T is published over T1                    (TS)
-// The elementwise groups compute P^T while dP^T is still in the tensor
-// pipe and dS^T while dV runs.  S^T of the next iteration is issued once dV
-// has read P^T (done[0]), dP^T once dK has read dS^T (done[1]); both are
-// then queued behind the MMA still running.
+// Issue order in steady state:  dV(it), S^T(it+1), dK(it), dP^T(it+1).
+// S^T(it+1) may overwrite T0 once dV(it) has read P^T (done[0]) and runs
+// while the elementwise groups compute dS^T(it); dP^T(it+1) may overwrite
+// T1 once dK(it) has read dS^T (done[1]) and runs while they compute
+// P^T(it+1).  Each wait thus has an MMA queued behind it.
 template <int D>
 __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatile int* abort,
                                               uint32_t tmem, int n_it) {
@@ -185,20 +186,21 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
-  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort);
-  for (int it = 0; ok && it < n_it; ++it) {
-    const int s0 = (2 * it) % C::NSTAGE, u0 = (2 * it) / C::NSTAGE;
-    const int s1 = (2 * it + 1) % C::NSTAGE, u1 = (2 * it + 1) / C::NSTAGE;
-    if (!(ok = tc::mbar_wait(&bars->ring_full[s0], u0 & 1, abort))) break;
-    if (!(ok = tc::mbar_wait(&bars->ring_full[s1], u1 & 1, abort))) break;
-    if (it > 0 && !(ok = tc::mbar_wait(&bars->done[0], (it - 1) & 1, abort))) break;
+  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort) &&
+            tc::mbar_wait(&bars->ring_full[0], 0, abort) &&
+            tc::mbar_wait(&bars->ring_full[1], 0, abort);
+  if (ok) {
     tc::fence_after_sync();
-    mma_tile_ss<D>(tmem + T0, fix, ring + s0 * C::TILE);
+    mma_tile_ss<D>(tmem + T0, fix, ring);
     tc::mma_commit(&bars->sd_full);
-    if (it > 0 && !(ok = tc::mbar_wait(&bars->done[1], (it - 1) & 1, abort))) break;
-    tc::fence_after_sync();
-    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + s1 * C::TILE);
+    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + C::TILE);
     tc::mma_commit(&bars->dp_full);
+  }
+  for (int it = 0; ok && it < n_it; ++it) {
+    const int s0 = (2 * it) % C::NSTAGE, s1 = (2 * it + 1) % C::NSTAGE;
+    const int n0 = (2 * it + 2) % C::NSTAGE, n1 = (2 * it + 3) % C::NSTAGE;
+    const bool more = it + 1 < n_it;
+    // dV(it) += P^T(it) dO(it)
     if (!(ok = tc::mbar_wait(&bars->p_full[0], it & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
@@ -207,6 +209,15 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
                  tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
     tc::mma_commit(&bars->done[0]);
+    // S^T(it+1) once dV(it) has read P^T(it)
+    if (more) {
+      if (!(ok = tc::mbar_wait(&bars->ring_full[n0], ((2 * it + 2) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait(&bars->done[0], it & 1, abort))) break;
+      tc::fence_after_sync();
+      mma_tile_ss<D>(tmem + T0, fix, ring + n0 * C::TILE);
+      tc::mma_commit(&bars->sd_full);
+    }
+    // dK(it) += dS^T(it) Q(it)
     if (!(ok = tc::mbar_wait(&bars->p_full[1], it & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
@@ -217,6 +228,14 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
     tc::mma_commit(&bars->done[1]);
     tc::mma_commit(&bars->ring_empty[s0]);
     tc::mma_commit(&bars->ring_empty[s1]);
+    // dP^T(it+1) once dK(it) has read dS^T(it)
+    if (more) {
+      if (!(ok = tc::mbar_wait(&bars->ring_full[n1], ((2 * it + 3) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait(&bars->done[1], it & 1, abort))) break;
+      tc::fence_after_sync();
+      mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
+      tc::mma_commit(&bars->dp_full);
+    }
   }
   if (!ok) {
     tc::mma_commit(&bars->drain);
