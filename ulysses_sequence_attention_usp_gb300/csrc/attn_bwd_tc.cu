@@ -57,10 +57,11 @@ struct Bars {
   uint64_t sd_full;       // dq: S and dP of the iteration computed; dkdv: S^T computed
   uint64_t dp_full;       // dkdv: dP^T computed
   uint64_t consumed;      // dq: both elementwise groups read S and dP (256 arrivals)
+  uint64_t q_ready;       // dq: the Q tile is in TMEM (256 arrivals)
   uint64_t p_full[2];     // dkdv: P^T published ([0]), dS^T published ([1]);
-                          // dq: dS written to buffer b ([b]); 256 arrivals each
+                          // dq: dS written ([0]); 256 arrivals each
   uint64_t done[2];       // dkdv: dV MMA done ([0]), dK MMA done ([1]);
-                          // dq: dQ MMA that read dS buffer b done ([b])
+                          // dq: dQ MMA that read dS done ([0])
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -69,6 +70,7 @@ struct Bars {
 struct Params {
   const int32_t* doc;
   const int32_t* cu;
+  const bf16* q;         // head-layout Q (the dQ pass keeps its Q tile in TMEM)
   const float* lse2;     // [P][hq][S_ws] LSE*log2(e); +inf for rows without keys
   const float* delta;    // [P][hq][S_ws] rowsum(dO*O); S_ws = S_pad rounded up to BT
   bf16* dq;
@@ -104,6 +106,7 @@ __device__ __forceinline__ void init_common(Bars* bars) {
   tc::mbar_init(&bars->sd_full, 1);
   tc::mbar_init(&bars->dp_full, 1);
   tc::mbar_init(&bars->consumed, 256);
+  tc::mbar_init(&bars->q_ready, 256);
   for (int b = 0; b < 2; ++b) {
     tc::mbar_init(&bars->p_full[b], 256);
     tc::mbar_init(&bars->done[b], 1);
@@ -125,9 +128,11 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int*
                                         const CUtensorMap* m1, int n_it, CoordFn coord,
                                         VecFn vec) {
   using C = Cfg<D>;
-  tc::mbar_expect_tx(&bars->fix_full, 2 * C::TILE);
+  // f0 == nullptr: only the second stationary tile is loaded
+  tc::mbar_expect_tx(&bars->fix_full, (f0 != nullptr ? 2 : 1) * C::TILE);
   for (int b = 0; b < C::NB; ++b) {
-    tc::tma_load_3d(smem + C::FIX_OFF + b * C::BOX, f0, &bars->fix_full, f0c0 + b * 64, fc1, g);
+    if (f0 != nullptr)
+      tc::tma_load_3d(smem + C::FIX_OFF + b * C::BOX, f0, &bars->fix_full, f0c0 + b * 64, fc1, g);
     tc::tma_load_3d(smem + C::FIX_OFF + C::TILE + b * C::BOX, f1, &bars->fix_full, f1c0 + b * 64,
                     fc1, g);
   }
@@ -243,27 +248,40 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
   }
 }
 
-// dQ MMA issuer.  Iteration j streams key tile K_j (R0) and V_j (R1):
-//   S(j) = Q K_j^T (T0),  dP(j) = dO V_j^T (T1)          (SS)
-//   dQ += dS(j) K_j   with dS(j) in TMEM buffer j%2       (TS, K = 128)
+// dQ MMA issuer.  The Q tile of this CTA sits in TMEM (columns QC..QC+63,
+// written once by the elementwise groups), so S needs no shared-memory
+// reads for its A operand.  Iteration j streams key tile K_j (R0), V_j (R1):
+//   S(j) = Q K_j^T (T0, TS),  dP(j) = dO V_j^T (T1, SS)
+//   dQ += dS(j) K_j   with dS(j) in TMEM columns R..R+63              (TS)
 // S(j+1) and dP(j+1) are issued as soon as the elementwise groups have read
 // S(j) and dP(j) ("consumed"), before they finish dS(j), so the tensor pipe
-// keeps working while they compute.  Buffer b of dS is rewritten for j+2
-// only after done[b] (the dQ MMA that read it).
+// keeps working while they compute.  The dS columns are rewritten for j+1
+// only after done[0] of dQ(j).
+template <int D>
+__device__ __forceinline__ void mma_tile_s_ts(uint32_t d_tmem, uint32_t q_tmem, uint32_t k) {
+  using C = Cfg<D>;
+  constexpr uint32_t id = tc::idesc_bf16(128, BT, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
+    tc::mma_ts(d_tmem, q_tmem + 8 * kk, tc::desc_sw128(k + off, 16, 1024), id, kk > 0);
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile int* abort,
                                             uint32_t tmem, int n_it) {
   using C = Cfg<D>;
-  constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, R = 384;
+  constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, R = 384, QC = 448;
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
-  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort) &&
+  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort) && tc::mbar_wait(&bars->q_ready, 0, abort) &&
             tc::mbar_wait(&bars->ring_full[0], 0, abort) &&
             tc::mbar_wait(&bars->ring_full[1], 0, abort);
   if (ok) {
     tc::fence_after_sync();
-    mma_tile_ss<D>(tmem + T0, fix, ring);
+    mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring);
     mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + C::TILE);
     tc::mma_commit(&bars->sd_full);
   }
@@ -275,19 +293,18 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
       if (!(ok = tc::mbar_wait(&bars->ring_full[n0], ((2 * j + 2) / C::NSTAGE) & 1, abort))) break;
       if (!(ok = tc::mbar_wait(&bars->ring_full[n1], ((2 * j + 3) / C::NSTAGE) & 1, abort))) break;
       tc::fence_after_sync();
-      mma_tile_ss<D>(tmem + T0, fix, ring + n0 * C::TILE);
+      mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring + n0 * C::TILE);
       mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
       tc::mma_commit(&bars->sd_full);
     }
-    const int b = j & 1;
-    if (!(ok = tc::mbar_wait(&bars->p_full[b], (j >> 1) & 1, abort))) break;
+    if (!(ok = tc::mbar_wait(&bars->p_full[0], j & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-      tc::mma_ts(tmem + A0, tmem + R + 64 * b + 8 * kk,
+      tc::mma_ts(tmem + A0, tmem + R + 8 * kk,
                  tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (j > 0 || kk > 0) ? 1u : 0u);
-    tc::mma_commit(&bars->done[b]);
+    tc::mma_commit(&bars->done[0]);
     tc::mma_commit(&bars->ring_empty[s0]);
     tc::mma_commit(&bars->ring_empty[s1]);
   }
@@ -358,7 +375,7 @@ __device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, int h, const float* d
 
 // dQ elementwise work on half h (keys [64h, 64h+64)) of this thread's query
 // row: read S and dP, let the MMA issuer reuse them ("consumed"), compute
-// dS = exp2(S*sl2 - lse2) (dP - delta) and, once dS buffer `b` is free,
+// dS = exp2(S*sl2 - lse2) (dP - delta) and, once the dS columns are free,
 // write it there as bf16 (32 columns: K steps 4h..4h+3).
 template <bool MASK>
 __device__ __forceinline__ bool dq_half(uint32_t tS, uint32_t tP, uint32_t tR, int h, int lo,
@@ -385,8 +402,8 @@ __device__ __forceinline__ bool dq_half(uint32_t tS, uint32_t tP, uint32_t tR, i
     }
     w[i] = tc::pack_bf16(dd[0], dd[1]);
   }
-  if (j >= 2) {   // the dQ MMA of iteration j-2 read this buffer
-    if (!__all_sync(0xffffffffu, tc::mbar_wait(&bars->done[j & 1], ((j >> 1) - 1) & 1, abort)))
+  if (j >= 1) {   // the dQ MMA of iteration j-1 read the dS columns
+    if (!__all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], (j - 1) & 1, abort)))
       return false;
     tc::fence_after_sync();
   }
@@ -578,7 +595,7 @@ __global__ void __launch_bounds__(384, 1)
       tc::prefetch_tmap(&tmK);
       tc::prefetch_tmap(&tmV);
       produce<D, false>(
-          smem, bars, abort, &tmQ, jq * D, &tmdO, jq * D, (int)t0, g, &tmK, &tmV, n_kv,
+          smem, bars, abort, nullptr, 0, &tmdO, jq * D, (int)t0, g, &tmK, &tmV, n_kv,
           [&](int it, int, int& c0, int& c1) {
             c0 = jk * D;
             c1 = (int)(kv_start + (int64_t)it * BT);
@@ -602,6 +619,23 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
     const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
     bool ok = true;
+    // this thread's Q row, columns [64*half, 64*half + 64), into TMEM as
+    // the A operand of S = Q K^T (bf16 pairs, 32 columns)
+    {
+      uint32_t qw[32];
+      const bool mine = D == 128 || half == 0;     // D = 64: the left group holds the row
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + (((int64_t)g * p.S_pad + t) * p.hq + jq) * D + (mine ? 64 * half : 0));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = (t < p.S_pad && mine) ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
+      }
+      if (D == 128 || half == 0) tc::tmem_st_x32(tc::tmem_addr(tmem, quarter * 32, 448 + 32 * half), qw);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->q_ready);
+    }
     const uint32_t tR = tc::tmem_addr(tmem, quarter * 32, 384);
     for (int it = 0; it < n_kv; ++it) {
       ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full, it & 1, abort));
@@ -611,17 +645,16 @@ __global__ void __launch_bounds__(384, 1)
       const int lo = (int)max((int64_t)0, min((int64_t)BT, ds - u0));
       const int hi = ds < 0 ? -1 : (int)min((int64_t)BT - 1, t - u0);
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
-      const uint32_t tRb = tR + 64 * (it & 1);
+      const uint32_t tRb = tR;
       ok = mask ? dq_half<true>(tS, tP, tRb, half, lo, hi, lse2, dl, p.scale_log2, bars, it, abort)
                 : dq_half<false>(tS, tP, tRb, half, lo, hi, lse2, dl, p.scale_log2, bars, it, abort);
       if (!ok) break;
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      tc::mbar_arrive(&bars->p_full[it & 1]);
+      tc::mbar_arrive(&bars->p_full[0]);
     }
-    if (ok && n_kv > 0) {
-      const int jl = n_kv - 1;   // the last dQ MMA completes after all earlier ones
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[jl & 1], (jl >> 1) & 1, abort));
+    if (ok && n_kv > 0) {   // the last dQ MMA completes after all earlier ones
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], (n_kv - 1) & 1, abort));
       tc::fence_after_sync();
     }
     const bool have = ok && n_kv > 0;
@@ -757,6 +790,7 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
   Params prm;
   prm.doc = doc;
   prm.cu = cu;
+  prm.q = reinterpret_cast<const bf16*>(q);
   float* delta = reinterpret_cast<float*>(ws);
   float* lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + vec_bytes(g));
   prm.lse2 = lse2;
