@@ -37,18 +37,25 @@ using bf16 = __nv_bfloat16;
 constexpr int BT = 128;                       // rows per tile (queries and keys)
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
-struct Cfg {
+// Shared-memory plan: NFIX stationary tiles, a ring of NS streamed tiles
+// (two per iteration), barriers, and (VEC) 128 fp32 staged next to each
+// ring slot.
+template <int D, int NFIX, int NS, bool VEC>
+struct CfgT {
   static constexpr int NB = D / 64;
   static constexpr int BOX = 128 * 128;
   static constexpr int TILE = NB * BOX;
-  static constexpr int NSTAGE = 4;            // ring slots (two per iteration)
-  static constexpr int FIX_OFF = 0;           // two stationary tiles
-  static constexpr int RING_OFF = 2 * TILE;
+  static constexpr int NSTAGE = NS;
+  static constexpr int FIX_OFF = 0;
+  static constexpr int RING_OFF = NFIX * TILE;
   static constexpr int BAR_OFF = RING_OFF + NSTAGE * TILE;
-  static constexpr int VEC_OFF = BAR_OFF + 512;   // per ring slot: 128 fp32 (dkdv)
-  static constexpr int SMEM = VEC_OFF + NSTAGE * BT * 4 + 1024;
+  static constexpr int VEC_OFF = BAR_OFF + 512;
+  static constexpr int SMEM = VEC_OFF + (VEC ? NSTAGE * BT * 4 : 0) + 1024;
 };
+// dK/dV: K and V stationary, Q/dO streamed with LSE*log2(e)/delta vectors.
+template <int D> using CfgKV = CfgT<D, 2, 4, true>;
+// dQ: dO stationary (Q lives in TMEM), K/V streamed through six slots.
+template <int D> using CfgQ = CfgT<D, 1, 6, false>;
 
 struct Bars {
   uint64_t fix_full;
@@ -95,9 +102,8 @@ __device__ __forceinline__ int64_t doc_end_of(const Params& p, int64_t t) {
   return p.cu ? (int64_t)__ldg(p.cu + d + 1) : p.S;
 }
 
-template <int D>
+template <class C>
 __device__ __forceinline__ void init_common(Bars* bars) {
-  using C = Cfg<D>;
   tc::mbar_init(&bars->fix_full, 1);
   for (int s = 0; s < C::NSTAGE; ++s) {
     tc::mbar_init(&bars->ring_full[s], 1);
@@ -121,20 +127,20 @@ __device__ __forceinline__ void init_common(Bars* bars) {
 // the coordinates of streamed tile w of iteration it (map m0 or m1).  With
 // VEC, vec(it, w) also names 128 fp32 values copied next to the tile (into
 // the slot's vector area; 512 bytes, 16-byte aligned).
-template <int D, bool VEC, typename CoordFn, typename VecFn>
+template <class C, bool VEC, typename CoordFn, typename VecFn>
 __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int* abort,
                                         const CUtensorMap* f0, int f0c0, const CUtensorMap* f1,
                                         int f1c0, int fc1, int g, const CUtensorMap* m0,
                                         const CUtensorMap* m1, int n_it, CoordFn coord,
                                         VecFn vec) {
-  using C = Cfg<D>;
-  // f0 == nullptr: only the second stationary tile is loaded
-  tc::mbar_expect_tx(&bars->fix_full, (f0 != nullptr ? 2 : 1) * C::TILE);
+  // f0 == nullptr: only f1 is loaded, into stationary tile 0
+  const int nf = f0 != nullptr ? 2 : 1;
+  tc::mbar_expect_tx(&bars->fix_full, nf * C::TILE);
   for (int b = 0; b < C::NB; ++b) {
     if (f0 != nullptr)
       tc::tma_load_3d(smem + C::FIX_OFF + b * C::BOX, f0, &bars->fix_full, f0c0 + b * 64, fc1, g);
-    tc::tma_load_3d(smem + C::FIX_OFF + C::TILE + b * C::BOX, f1, &bars->fix_full, f1c0 + b * 64,
-                    fc1, g);
+    tc::tma_load_3d(smem + C::FIX_OFF + (nf - 1) * C::TILE + b * C::BOX, f1, &bars->fix_full,
+                    f1c0 + b * 64, fc1, g);
   }
   int issued = 0;
   for (int it = 0; it < n_it && !*abort; ++it) {
@@ -162,9 +168,9 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int*
 
 // Issue T = F x R^T for one 128x128 tile pair (SS, K-major operands, K = D):
 // F is a stationary tile, R a ring tile.
-template <int D>
+template <class C>
 __device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint32_t f, uint32_t r) {
-  using C = Cfg<D>;
+  constexpr int D = C::NB * 64;
   constexpr uint32_t id = tc::idesc_bf16(128, BT, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
@@ -186,7 +192,7 @@ __device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint32_t f, uint32_
 template <int D>
 __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatile int* abort,
                                               uint32_t tmem, int n_it) {
-  using C = Cfg<D>;
+  using C = CfgKV<D>;
   constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, A1 = 256 + D;
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
@@ -196,9 +202,9 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
             tc::mbar_wait(&bars->ring_full[1], 0, abort);
   if (ok) {
     tc::fence_after_sync();
-    mma_tile_ss<D>(tmem + T0, fix, ring);
+    mma_tile_ss<C>(tmem + T0, fix, ring);
     tc::mma_commit(&bars->sd_full);
-    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + C::TILE);
+    mma_tile_ss<C>(tmem + T1, fix + C::TILE, ring + C::TILE);
     tc::mma_commit(&bars->dp_full);
   }
   for (int it = 0; ok && it < n_it; ++it) {
@@ -219,7 +225,7 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
       if (!(ok = tc::mbar_wait(&bars->ring_full[n0], ((2 * it + 2) / C::NSTAGE) & 1, abort))) break;
       if (!(ok = tc::mbar_wait(&bars->done[0], it & 1, abort))) break;
       tc::fence_after_sync();
-      mma_tile_ss<D>(tmem + T0, fix, ring + n0 * C::TILE);
+      mma_tile_ss<C>(tmem + T0, fix, ring + n0 * C::TILE);
       tc::mma_commit(&bars->sd_full);
     }
     // dK(it) += dS^T(it) Q(it)
@@ -238,7 +244,7 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
       if (!(ok = tc::mbar_wait(&bars->ring_full[n1], ((2 * it + 3) / C::NSTAGE) & 1, abort))) break;
       if (!(ok = tc::mbar_wait(&bars->done[1], it & 1, abort))) break;
       tc::fence_after_sync();
-      mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
+      mma_tile_ss<C>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
       tc::mma_commit(&bars->dp_full);
     }
   }
@@ -259,7 +265,7 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
 // only after done[0] of dQ(j).
 template <int D>
 __device__ __forceinline__ void mma_tile_s_ts(uint32_t d_tmem, uint32_t q_tmem, uint32_t k) {
-  using C = Cfg<D>;
+  using C = CfgQ<D>;
   constexpr uint32_t id = tc::idesc_bf16(128, BT, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
@@ -271,7 +277,7 @@ __device__ __forceinline__ void mma_tile_s_ts(uint32_t d_tmem, uint32_t q_tmem, 
 template <int D>
 __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile int* abort,
                                             uint32_t tmem, int n_it) {
-  using C = Cfg<D>;
+  using C = CfgQ<D>;
   constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, R = 384, QC = 448;
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
@@ -282,8 +288,9 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
   if (ok) {
     tc::fence_after_sync();
     mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring);
-    mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + C::TILE);
+    mma_tile_ss<C>(tmem + T1, fix, ring + C::TILE);
     tc::mma_commit(&bars->sd_full);
+    tc::mma_commit(&bars->ring_empty[1]);      // V_0 is only read by dP(0)
   }
   for (int j = 0; ok && j < n_it; ++j) {
     const int s0 = (2 * j) % C::NSTAGE, s1 = (2 * j + 1) % C::NSTAGE;
@@ -294,8 +301,9 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
       if (!(ok = tc::mbar_wait(&bars->ring_full[n1], ((2 * j + 3) / C::NSTAGE) & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring + n0 * C::TILE);
-      mma_tile_ss<D>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
+      mma_tile_ss<C>(tmem + T1, fix, ring + n1 * C::TILE);
       tc::mma_commit(&bars->sd_full);
+      tc::mma_commit(&bars->ring_empty[n1]);   // V_{j+1} is only read by dP(j+1)
     }
     if (!(ok = tc::mbar_wait(&bars->p_full[0], j & 1, abort))) break;
     tc::fence_after_sync();
@@ -305,8 +313,8 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
                  tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (j > 0 || kk > 0) ? 1u : 0u);
     tc::mma_commit(&bars->done[0]);
-    tc::mma_commit(&bars->ring_empty[s0]);
-    tc::mma_commit(&bars->ring_empty[s1]);
+    tc::mma_commit(&bars->ring_empty[s0]);     // K_j: read by S(j) and dQ(j)
+    (void)s1;                                   // V_j was released after dP(j)
   }
   if (!ok) {
     tc::mma_commit(&bars->drain);
@@ -428,7 +436,7 @@ __global__ void __launch_bounds__(384, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const Params p) {
-  using C = Cfg<D>;
+  using C = CfgKV<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -452,7 +460,7 @@ __global__ void __launch_bounds__(384, 1)
   }
   const int n_it = n_q * p.G;    // iteration it: query tile it / G, head jk*G + it % G
 
-  if (threadIdx.x == 0) init_common<D>(bars);
+  if (threadIdx.x == 0) init_common<C>(bars);
   if (warp == 1) {
     tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
@@ -467,7 +475,7 @@ __global__ void __launch_bounds__(384, 1)
       tc::prefetch_tmap(&tmQ);
       tc::prefetch_tmap(&tmdO);
       const int G = p.G;
-      produce<D, true>(
+      produce<C, true>(
           smem, bars, abort, &tmK, jk * D, &tmV, jk * D, (int)u0, g, &tmQ, &tmdO, n_it,
           [&](int it, int, int& c0, int& c1) {
             c0 = (jk * G + it % G) * D;
@@ -557,7 +565,7 @@ __global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const Params p) {
-  using C = Cfg<D>;
+  using C = CfgQ<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -580,7 +588,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
 
-  if (threadIdx.x == 0) init_common<D>(bars);
+  if (threadIdx.x == 0) init_common<C>(bars);
   if (warp == 1) {
     tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
@@ -594,7 +602,7 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0 && n_kv > 0) {
       tc::prefetch_tmap(&tmK);
       tc::prefetch_tmap(&tmV);
-      produce<D, false>(
+      produce<C, false>(
           smem, bars, abort, nullptr, 0, &tmdO, jq * D, (int)t0, g, &tmK, &tmV, n_kv,
           [&](int it, int, int& c0, int& c1) {
             c0 = jk * D;
@@ -743,7 +751,6 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
                        const CUtensorMap& mv, const CUtensorMap& mdo, const Params& prm,
                        const bf16* o, const bf16* dout, const float* lse, float* delta,
                        float* lse2, cudaStream_t st) {
-  using C = Cfg<D>;
   const int64_t n_rows = (int64_t)g.P * g.S_pad * g.hq;
   int64_t blocks = (n_rows * (D / 8) * 1 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
@@ -751,16 +758,18 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
                                                                  g.S_pad, prm.S_ws, g.hq, n_rows);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  constexpr int smem_kv = CfgKV<D>::SMEM, smem_q = CfgQ<D>::SMEM;
+  static_assert(smem_kv <= 232448 && smem_q <= 232448, "shared memory plan too large");
   if ((e = cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::SMEM)) != cudaSuccess)
+                                smem_kv)) != cudaSuccess)
     return e;
   if ((e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::SMEM)) != cudaSuccess)
+                                smem_q)) != cudaSuccess)
     return e;
-  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), 384, C::SMEM, st>>>(
+  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), 384, smem_kv, st>>>(
       mq, mk, mv, mdo, prm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), 384, C::SMEM, st>>>(
+  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), 384, smem_q, st>>>(
       mq, mk, mv, mdo, prm);
   usp_count_launches(3);
   return cudaGetLastError();

@@ -48,6 +48,7 @@ struct Cfg {
   static constexpr int KV_OFF = NH * TILE;
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE;
   static constexpr int SMEM = BAR_OFF + 512 + 1024;   // barriers + alignment slack
+  static_assert(SMEM <= 232448, "shared memory plan too large");
   // TMEM columns: S/P of slot h at h*128, O of slot h at 256 + h*D
   static constexpr uint32_t S_COL(int h) { return h * 128; }
   static constexpr uint32_t O_COL(int h) { return 256 + h * D; }
