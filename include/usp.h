@@ -226,6 +226,17 @@ usp_status usp_rope_table(int64_t n_pos, int32_t D, double base, double yarn_fac
  */
 usp_status usp_device_status(void* stream);
 
+/*
+ * usp_selftest_bounded_wait -- diagnostic for the failure-detection path:
+ * launches one CTA whose thread waits, exactly as the attention kernels
+ * wait, on an mbarrier that nothing completes, giving up after limit_us
+ * microseconds (1..1000000; USP_ERR_INVALID_ARG otherwise).  The CTA then
+ * records a timeout in the device status word and exits, so the next
+ * usp_device_status() returns USP_ERR_TIMEOUT (and clears it) while the
+ * CUDA context stays usable.  Nothing traps, faults or hangs.
+ */
+usp_status usp_selftest_bounded_wait(int32_t limit_us, void* stream);
+
 const char* usp_status_string(usp_status s);
 int usp_abi_version(void);
 

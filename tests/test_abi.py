@@ -124,3 +124,8 @@ def test_library_rope_table_matches_oracle(n, D, base, f, L):
     diff = a.view(np.int32).astype(np.int64) - b.view(np.int32).astype(np.int64)
     assert np.max(np.abs(diff)) <= 1
     assert np.count_nonzero(diff) <= max(2, a.size // 10**6)
+
+
+def test_selftest_wait_limit_validated_on_host():
+    assert B.raw_call("usp_selftest_bounded_wait", 0, None) == 1
+    assert B.raw_call("usp_selftest_bounded_wait", 2000000, None) == 1

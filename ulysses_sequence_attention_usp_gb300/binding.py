@@ -57,6 +57,7 @@ _SIGS = {
     "usp_head_to_seq": [_DIMS, _P, _I32, _P, _P, _I64, _I32, _P, _P],
     "usp_rope_table": [_I64, _I32, ctypes.c_double, ctypes.c_double, _I32, _P],
     "usp_device_status": [_P],
+    "usp_selftest_bounded_wait": [_I32, _P],
 }
 for _name, _args in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -174,6 +175,11 @@ def usp_rope_table(n_pos, D, base, yarn_factor=1.0, yarn_orig_ctx=0):
 
 def usp_device_status(stream=None):
     _check(_lib.usp_device_status(_stream(stream)), "usp_device_status")
+
+
+def usp_selftest_bounded_wait(limit_us, stream=None):
+    _check(_lib.usp_selftest_bounded_wait(int(limit_us), _stream(stream)),
+           "usp_selftest_bounded_wait")
 
 
 def usp_status_string(status: int) -> str:

@@ -224,31 +224,34 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, true);
       const uint32_t q_base = tc::smem_u32(smem + C::Q_OFF);
       const uint32_t kv_base = tc::smem_u32(smem + C::KV_OFF);
-      bool ok = tc::mbar_wait(&bars->q_full, 0, abort);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int sk = (2 * j) % C::NSTAGE, uk = (2 * j) / C::NSTAGE;
-        if (!(ok = tc::mbar_wait(&bars->kv_full[sk], uk & 1, abort))) break;
-        tc::fence_after_sync();
-        for (int h = 0; h < NH && ok; ++h) {
-          if (j > 0) {
-            // S_h aliases P_h: the previous P V must have read it
-            if (!(ok = tc::mbar_wait(&bars->o_full[h], (j - 1) & 1, abort))) break;
-            tc::fence_after_sync();
-          }
+      // S_h = Q_h K^T for key tile `kt` (ring slot `sk`)
+      auto issue_qk = [&](int h, int sk) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
-            const uint64_t da = tc::desc_sw128(q_base + h * C::TILE + off, 16, 1024);
-            const uint64_t db = tc::desc_sw128(kv_base + sk * C::TILE + off, 16, 1024);
-            tc::mma_ss(tmem + C::S_COL(h), da, db, idesc_qk, kk > 0);
-          }
-          tc::mma_commit(&bars->s_full[h]);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
+          const uint64_t da = tc::desc_sw128(q_base + h * C::TILE + off, 16, 1024);
+          const uint64_t db = tc::desc_sw128(kv_base + sk * C::TILE + off, 16, 1024);
+          tc::mma_ss(tmem + C::S_COL(h), da, db, idesc_qk, kk > 0);
         }
-        if (!ok) break;
-        tc::mma_commit(&bars->kv_empty[sk]);
-        const int sv = (2 * j + 1) % C::NSTAGE, uv = (2 * j + 1) / C::NSTAGE;
-        if (!(ok = tc::mbar_wait(&bars->kv_full[sv], uv & 1, abort))) break;
+        tc::mma_commit(&bars->s_full[h]);
+      };
+      // Issue order: QK_0(0) QK_1(0), then per key tile j
+      //   PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1)
+      // QK_h(j+1) rewrites S_h, which holds P_h(j): it waits for PV_h(j) to
+      // complete (o_full[h]).  Each head's softmax of tile j+1 then overlaps
+      // the other head's PV and QK (two MMA groups) instead of one.
+      bool ok = tc::mbar_wait(&bars->q_full, 0, abort) &&
+                tc::mbar_wait(&bars->kv_full[0], 0, abort);
+      if (ok) {
         tc::fence_after_sync();
+        for (int h = 0; h < NH; ++h) issue_qk(h, 0);
+        tc::mma_commit(&bars->kv_empty[0]);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int sv = (2 * j + 1) % C::NSTAGE, uv = (2 * j + 1) / C::NSTAGE;
+        const int sk = (2 * j + 2) % C::NSTAGE, uk = (2 * j + 2) / C::NSTAGE;
+        const bool more = j + 1 < n_kv;
+        if (!(ok = tc::mbar_wait(&bars->kv_full[sv], uv & 1, abort))) break;
         for (int h = 0; h < NH && ok; ++h) {
           if (!(ok = tc::mbar_wait(&bars->p_full[h], j & 1, abort))) break;
           tc::fence_after_sync();
@@ -259,9 +262,15 @@ __global__ void __launch_bounds__(384, 1)
                        (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc::mma_commit(&bars->o_full[h]);
+          if (h == NH - 1) tc::mma_commit(&bars->kv_empty[sv]);
+          if (more) {
+            if (!(ok = tc::mbar_wait(&bars->kv_full[sk], uk & 1, abort))) break;
+            if (!(ok = tc::mbar_wait(&bars->o_full[h], j & 1, abort))) break;
+            tc::fence_after_sync();
+            issue_qk(h, sk);
+            if (h == NH - 1) tc::mma_commit(&bars->kv_empty[sk]);
+          }
         }
-        if (!ok) break;
-        tc::mma_commit(&bars->kv_empty[sv]);
       }
       if (!ok) {
         // wait (bounded) for the MMAs already issued before TMEM is freed

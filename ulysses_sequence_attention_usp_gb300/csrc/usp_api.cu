@@ -267,6 +267,13 @@ usp_status usp_rope_table(int64_t n_pos, int32_t D, double base, double yarn_fac
   return USP_OK;
 }
 
+usp_status usp_selftest_bounded_wait(int32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return USP_ERR_INVALID_ARG;
+  unsigned* word = status_word();
+  if (word == nullptr) return USP_ERR_CUDA;
+  return cuda_status(usp_launch_bounded_wait((int64_t)limit_us * 1000, word, (cudaStream_t)stream));
+}
+
 usp_status usp_device_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return USP_ERR_CUDA;

@@ -49,6 +49,8 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
                                 void* dq, void* dk, void* dv, void* ws, cudaStream_t st);
 size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g);
 
+cudaError_t usp_launch_bounded_wait(int64_t limit_ns, unsigned* status, cudaStream_t st);
+
 // Fixed backward scratch for usp_attn_bwd_noalloc (attn_bwd_tc.cu).
 size_t usp_noalloc_scratch_capacity();
 cudaError_t usp_noalloc_scratch(void** ptr);
