@@ -58,6 +58,50 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def kernel_source_hash(names):
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "ulysses_sequence_attention_usp_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+BWD_SOURCES = ["attn_bwd_tc.cu", "tc_ptx.cuh", "usp_common.cuh"]
+
+
+def measured_traffic(workload):
+    """DRAM bytes per usp_attn_bwd call from the committed ncu summary, or
+    None when the kernels changed since those counters were taken."""
+    p = os.path.join(ROOT, "profiles", "attn_bwd_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("workload") != workload or d.get("source_sha256") != kernel_source_hash(BWD_SOURCES):
+        return None
+    return d.get("dram_bytes_per_call")
+
+
+def reduce_max(value, world, device=None):
+    """Max of a per-rank float over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(world, tokens_per_rank, steps, seconds):
+    """Whole-job tokens/s: every rank runs the same workload (replicas), so
+    the job processes world * tokens * steps tokens in the slowest rank's
+    time."""
+    return world * tokens_per_rank * steps / seconds
+
+
 def causal_pairs(S, cu):
     if cu is None:
         return S * (S + 1) // 2
@@ -288,10 +332,7 @@ def run_usp(args, wl, inp):
     elapsed = t_start.elapsed_time(t_end) / 1e3
     stage_ms = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
                 for j, n in enumerate(stage_names)}
-    if world > 1:
-        tt = torch.tensor([elapsed], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed = float(tt.item())
+    elapsed = reduce_max(elapsed, world, dev)
 
     # ---- end to end through the public API with host buffers
     pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory()  # noqa: E731
@@ -317,11 +358,7 @@ def run_usp(args, wl, inp):
     b_ev.record(st)
     barrier()
     ua.check(st)
-    e2e_t = a_ev.elapsed_time(b_ev) / 1e3
-    if world > 1:
-        tt = torch.tensor([e2e_t], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_t = float(tt.item())
+    e2e_t = reduce_max(a_ev.elapsed_time(b_ev) / 1e3, world, dev)
     h2d = sum(a.nbytes for a in (inp.q, inp.k, inp.v, inp.do))
     d2h = sum(t.numel() * 2 for t in (ua.o, ua.dq, ua.dk, ua.dv))
 
@@ -331,7 +368,7 @@ def run_usp(args, wl, inp):
         f_fwd = 4.0 * wl.D * wl.Hq * pairs
         f_bwd = 10.0 * wl.D * wl.Hq * pairs
         step_s = elapsed / args.steps
-        value = world * wl.S * args.steps / elapsed
+        value = aggregate_throughput(world, wl.S, args.steps, elapsed)
         t_fwd = stage_ms["attn_fwd"] / 1e3
         t_bwd = stage_ms["attn_bwd"] / 1e3
         bq = wl.S_pad * wl.Hq * wl.D * 2
@@ -353,9 +390,11 @@ def run_usp(args, wl, inp):
                                            if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
                        "parallelism": f"replicas x{world} (P={wl.P} virtual shards per GPU)",
                        "l2": "inputs larger than L2 (Q alone %.2f GB); no flush" % (bq / 1e9)},
-            "roofline": {"kernel": "usp_attn_bwd", "bound": "tensor", "achieved": bwd_tf,
+            "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
+                         "bound": "tensor", "achieved": bwd_tf,
                          "peak": peak_t, "unit": "TFLOP/s", "frac": bwd_tf / peak_t,
-                         "traffic": None, "peak_source": f"{src} (sustained bf16)",
+                         "traffic": measured_traffic(wl.name),
+                         "peak_source": f"{src} (sustained bf16)",
                          "flops_per_launch": f_bwd},
             "attention": {"fwd_tflops": f_fwd / t_fwd / 1e12, "bwd_tflops": bwd_tf,
                           "fwd_frac": f_fwd / t_fwd / 1e12 / peak_t,
@@ -367,7 +406,7 @@ def run_usp(args, wl, inp):
                        "bytes_per_step": sum(rep_bytes.values())},
             "stage_ms": stage_ms,
             "gpu_launches": launches,
-            "e2e": {"value": world * wl.S * e2e_steps / e2e_t, "unit": "tokens/s",
+            "e2e": {"value": aggregate_throughput(world, wl.S, e2e_steps, e2e_t), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "clocks": clk,
         }
