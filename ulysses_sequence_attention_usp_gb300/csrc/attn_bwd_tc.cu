@@ -21,7 +21,7 @@
 //                 key tiles:  S = Q K^T, dP = dO V^T (SS), dS over S (bf16),
 //                 dQ += dS K (TS).
 // Both reuse the forward's warp roles: warp 0 TMA producer, warp 1 TMEM
-// owner and MMA issuer; warps 4-7 and 8-11 do the per-row elementwise work
+// owner and MMA issuer (whole warp, one elected lane issues); warps 4-7 and 8-11 do the per-row elementwise work
 // on the left and right 64 columns of each tile (two warps per SM
 // sub-partition, so one hides the other's latency) and the epilogue.
 // The bf16 values of each 32-column chunk are written over the first 16
@@ -175,7 +175,7 @@ __device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint32_t f, uint32_
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
-    tc::mma_ss(d_tmem, tc::desc_sw128(f + off, 16, 1024), tc::desc_sw128(r + off, 16, 1024), id,
+    tc::mma_ss_w(d_tmem, tc::desc_sw128(f + off, 16, 1024), tc::desc_sw128(r + off, 16, 1024), id,
                kk > 0);
   }
 }
@@ -197,59 +197,59 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
-  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort) &&
-            tc::mbar_wait(&bars->ring_full[0], 0, abort) &&
-            tc::mbar_wait(&bars->ring_full[1], 0, abort);
+  bool ok = tc::mbar_wait_warp(&bars->fix_full, 0, abort) &&
+            tc::mbar_wait_warp(&bars->ring_full[0], 0, abort) &&
+            tc::mbar_wait_warp(&bars->ring_full[1], 0, abort);
   if (ok) {
     tc::fence_after_sync();
     mma_tile_ss<C>(tmem + T0, fix, ring);
-    tc::mma_commit(&bars->sd_full);
+    tc::mma_commit_w(&bars->sd_full);
     mma_tile_ss<C>(tmem + T1, fix + C::TILE, ring + C::TILE);
-    tc::mma_commit(&bars->dp_full);
+    tc::mma_commit_w(&bars->dp_full);
   }
   for (int it = 0; ok && it < n_it; ++it) {
     const int s0 = (2 * it) % C::NSTAGE, s1 = (2 * it + 1) % C::NSTAGE;
     const int n0 = (2 * it + 2) % C::NSTAGE, n1 = (2 * it + 3) % C::NSTAGE;
     const bool more = it + 1 < n_it;
     // dV(it) += P^T(it) dO(it)
-    if (!(ok = tc::mbar_wait(&bars->p_full[0], it & 1, abort))) break;
+    if (!(ok = tc::mbar_wait_warp(&bars->p_full[0], it & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-      tc::mma_ts(tmem + A0, tmem + T0 + 32 * (kk >> 1) + 8 * (kk & 1),
+      tc::mma_ts_w(tmem + A0, tmem + T0 + 32 * (kk >> 1) + 8 * (kk & 1),
                  tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
-    tc::mma_commit(&bars->done[0]);
+    tc::mma_commit_w(&bars->done[0]);
     // S^T(it+1) once dV(it) has read P^T(it)
     if (more) {
-      if (!(ok = tc::mbar_wait(&bars->ring_full[n0], ((2 * it + 2) / C::NSTAGE) & 1, abort))) break;
-      if (!(ok = tc::mbar_wait(&bars->done[0], it & 1, abort))) break;
+      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n0], ((2 * it + 2) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait_warp(&bars->done[0], it & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_ss<C>(tmem + T0, fix, ring + n0 * C::TILE);
-      tc::mma_commit(&bars->sd_full);
+      tc::mma_commit_w(&bars->sd_full);
     }
     // dK(it) += dS^T(it) Q(it)
-    if (!(ok = tc::mbar_wait(&bars->p_full[1], it & 1, abort))) break;
+    if (!(ok = tc::mbar_wait_warp(&bars->p_full[1], it & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-      tc::mma_ts(tmem + A1, tmem + T1 + 32 * (kk >> 1) + 8 * (kk & 1),
+      tc::mma_ts_w(tmem + A1, tmem + T1 + 32 * (kk >> 1) + 8 * (kk & 1),
                  tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
-    tc::mma_commit(&bars->done[1]);
-    tc::mma_commit(&bars->ring_empty[s0]);
-    tc::mma_commit(&bars->ring_empty[s1]);
+    tc::mma_commit_w(&bars->done[1]);
+    tc::mma_commit_w(&bars->ring_empty[s0]);
+    tc::mma_commit_w(&bars->ring_empty[s1]);
     // dP^T(it+1) once dK(it) has read dS^T(it)
     if (more) {
-      if (!(ok = tc::mbar_wait(&bars->ring_full[n1], ((2 * it + 3) / C::NSTAGE) & 1, abort))) break;
-      if (!(ok = tc::mbar_wait(&bars->done[1], it & 1, abort))) break;
+      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n1], ((2 * it + 3) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait_warp(&bars->done[1], it & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_ss<C>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
-      tc::mma_commit(&bars->dp_full);
+      tc::mma_commit_w(&bars->dp_full);
     }
   }
   if (!ok) {
-    tc::mma_commit(&bars->drain);
+    tc::mma_commit_w(&bars->drain);
     tc::mbar_wait(&bars->drain, 0, nullptr, 100000000ull);
   }
 }
@@ -270,7 +270,7 @@ __device__ __forceinline__ void mma_tile_s_ts(uint32_t d_tmem, uint32_t q_tmem, 
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
-    tc::mma_ts(d_tmem, q_tmem + 8 * kk, tc::desc_sw128(k + off, 16, 1024), id, kk > 0);
+    tc::mma_ts_w(d_tmem, q_tmem + 8 * kk, tc::desc_sw128(k + off, 16, 1024), id, kk > 0);
   }
 }
 
@@ -282,42 +282,43 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
-  bool ok = tc::mbar_wait(&bars->fix_full, 0, abort) && tc::mbar_wait(&bars->q_ready, 0, abort) &&
-            tc::mbar_wait(&bars->ring_full[0], 0, abort) &&
-            tc::mbar_wait(&bars->ring_full[1], 0, abort);
+  bool ok = tc::mbar_wait_warp(&bars->fix_full, 0, abort) &&
+            tc::mbar_wait_warp(&bars->q_ready, 0, abort) &&
+            tc::mbar_wait_warp(&bars->ring_full[0], 0, abort) &&
+            tc::mbar_wait_warp(&bars->ring_full[1], 0, abort);
   if (ok) {
     tc::fence_after_sync();
     mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring);
     mma_tile_ss<C>(tmem + T1, fix, ring + C::TILE);
-    tc::mma_commit(&bars->sd_full);
-    tc::mma_commit(&bars->ring_empty[1]);      // V_0 is only read by dP(0)
+    tc::mma_commit_w(&bars->sd_full);
+    tc::mma_commit_w(&bars->ring_empty[1]);      // V_0 is only read by dP(0)
   }
   for (int j = 0; ok && j < n_it; ++j) {
     const int s0 = (2 * j) % C::NSTAGE, s1 = (2 * j + 1) % C::NSTAGE;
-    if (!(ok = tc::mbar_wait(&bars->consumed, j & 1, abort))) break;
+    if (!(ok = tc::mbar_wait_warp(&bars->consumed, j & 1, abort))) break;
     if (j + 1 < n_it) {
       const int n0 = (2 * j + 2) % C::NSTAGE, n1 = (2 * j + 3) % C::NSTAGE;
-      if (!(ok = tc::mbar_wait(&bars->ring_full[n0], ((2 * j + 2) / C::NSTAGE) & 1, abort))) break;
-      if (!(ok = tc::mbar_wait(&bars->ring_full[n1], ((2 * j + 3) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n0], ((2 * j + 2) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n1], ((2 * j + 3) / C::NSTAGE) & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring + n0 * C::TILE);
       mma_tile_ss<C>(tmem + T1, fix, ring + n1 * C::TILE);
-      tc::mma_commit(&bars->sd_full);
-      tc::mma_commit(&bars->ring_empty[n1]);   // V_{j+1} is only read by dP(j+1)
+      tc::mma_commit_w(&bars->sd_full);
+      tc::mma_commit_w(&bars->ring_empty[n1]);   // V_{j+1} is only read by dP(j+1)
     }
-    if (!(ok = tc::mbar_wait(&bars->p_full[0], j & 1, abort))) break;
+    if (!(ok = tc::mbar_wait_warp(&bars->p_full[0], j & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-      tc::mma_ts(tmem + A0, tmem + R + 8 * kk,
+      tc::mma_ts_w(tmem + A0, tmem + R + 8 * kk,
                  tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (j > 0 || kk > 0) ? 1u : 0u);
-    tc::mma_commit(&bars->done[0]);
-    tc::mma_commit(&bars->ring_empty[s0]);     // K_j: read by S(j) and dQ(j)
+    tc::mma_commit_w(&bars->done[0]);
+    tc::mma_commit_w(&bars->ring_empty[s0]);     // K_j: read by S(j) and dQ(j)
     (void)s1;                                   // V_j was released after dP(j)
   }
   if (!ok) {
-    tc::mma_commit(&bars->drain);
+    tc::mma_commit_w(&bars->drain);
     tc::mbar_wait(&bars->drain, 0, nullptr, 100000000ull);
   }
 }
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(384, 1)
           });
     }
   } else if (warp == 1) {
-    if (lane == 0 && n_it > 0) mma_loop_dkdv<D>(smem, bars, abort, tmem, n_it);
+    if (n_it > 0) mma_loop_dkdv<D>(smem, bars, abort, tmem, n_it);   // whole warp
   } else if (warp >= 4) {
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)
@@ -611,7 +612,7 @@ __global__ void __launch_bounds__(384, 1)
           [&](int, int) -> const float* { return nullptr; });
     }
   } else if (warp == 1) {
-    if (lane == 0 && n_kv > 0) mma_loop_dq<D>(smem, bars, abort, tmem, n_kv);
+    if (n_kv > 0) mma_loop_dq<D>(smem, bars, abort, tmem, n_kv);     // whole warp
   } else if (warp >= 4) {
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)

@@ -11,7 +11,8 @@
 // Design (one CTA = 128 query rows x NH query heads that share one KV head):
 //   warp 0      TMA producer: Q tiles once, then K/V tiles through an
 //               NSTAGE-deep shared-memory ring (128-byte swizzle).
-//   warp 1      TMEM allocation and the single MMA-issuing thread:
+//   warp 1      TMEM allocation and MMA issue (the whole warp runs the
+//               loop, one elected lane issues each instruction):
 //               S_h = Q_h K^T (SS MMA, 128x128x D) into TMEM,
 //               O_h += P_h V   (TS MMA: P read from TMEM, V from smem).
 //   warps 4-7   softmax of head slot 0, warps 8-11 of slot 1: one thread
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_kv > 0) {
+    if (n_kv > 0) {                    // the whole warp; one lane issues
       constexpr uint32_t idesc_qk = tc::idesc_bf16(128, BN, false);
       constexpr uint32_t idesc_pv = tc::idesc_bf16(128, D, true);
       const uint32_t q_base = tc::smem_u32(smem + C::Q_OFF);
@@ -231,50 +232,50 @@ __global__ void __launch_bounds__(384, 1)
           const uint32_t off = (kk / 4) * C::BOX + (kk % 4) * 32;
           const uint64_t da = tc::desc_sw128(q_base + h * C::TILE + off, 16, 1024);
           const uint64_t db = tc::desc_sw128(kv_base + sk * C::TILE + off, 16, 1024);
-          tc::mma_ss(tmem + C::S_COL(h), da, db, idesc_qk, kk > 0);
+          tc::mma_ss_w(tmem + C::S_COL(h), da, db, idesc_qk, kk > 0);
         }
-        tc::mma_commit(&bars->s_full[h]);
+        tc::mma_commit_w(&bars->s_full[h]);
       };
       // Issue order: QK_0(0) QK_1(0), then per key tile j
       //   PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1)
       // QK_h(j+1) rewrites S_h, which holds P_h(j): it waits for PV_h(j) to
       // complete (o_full[h]).  Each head's softmax of tile j+1 then overlaps
       // the other head's PV and QK (two MMA groups) instead of one.
-      bool ok = tc::mbar_wait(&bars->q_full, 0, abort) &&
-                tc::mbar_wait(&bars->kv_full[0], 0, abort);
+      bool ok = tc::mbar_wait_warp(&bars->q_full, 0, abort) &&
+                tc::mbar_wait_warp(&bars->kv_full[0], 0, abort);
       if (ok) {
         tc::fence_after_sync();
         for (int h = 0; h < NH; ++h) issue_qk(h, 0);
-        tc::mma_commit(&bars->kv_empty[0]);
+        tc::mma_commit_w(&bars->kv_empty[0]);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const int sv = (2 * j + 1) % C::NSTAGE, uv = (2 * j + 1) / C::NSTAGE;
         const int sk = (2 * j + 2) % C::NSTAGE, uk = (2 * j + 2) / C::NSTAGE;
         const bool more = j + 1 < n_kv;
-        if (!(ok = tc::mbar_wait(&bars->kv_full[sv], uv & 1, abort))) break;
+        if (!(ok = tc::mbar_wait_warp(&bars->kv_full[sv], uv & 1, abort))) break;
         for (int h = 0; h < NH && ok; ++h) {
-          if (!(ok = tc::mbar_wait(&bars->p_full[h], j & 1, abort))) break;
+          if (!(ok = tc::mbar_wait_warp(&bars->p_full[h], j & 1, abort))) break;
           tc::fence_after_sync();
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk) {
             const uint64_t db = tc::desc_sw128(kv_base + sv * C::TILE + kk * 2048, C::BOX, 1024);
-            tc::mma_ts(tmem + C::O_COL(h), tmem + C::S_COL(h) + kk * 8, db, idesc_pv,
+            tc::mma_ts_w(tmem + C::O_COL(h), tmem + C::S_COL(h) + kk * 8, db, idesc_pv,
                        (j > 0 || kk > 0) ? 1u : 0u);
           }
-          tc::mma_commit(&bars->o_full[h]);
-          if (h == NH - 1) tc::mma_commit(&bars->kv_empty[sv]);
+          tc::mma_commit_w(&bars->o_full[h]);
+          if (h == NH - 1) tc::mma_commit_w(&bars->kv_empty[sv]);
           if (more) {
-            if (!(ok = tc::mbar_wait(&bars->kv_full[sk], uk & 1, abort))) break;
-            if (!(ok = tc::mbar_wait(&bars->o_full[h], j & 1, abort))) break;
+            if (!(ok = tc::mbar_wait_warp(&bars->kv_full[sk], uk & 1, abort))) break;
+            if (!(ok = tc::mbar_wait_warp(&bars->o_full[h], j & 1, abort))) break;
             tc::fence_after_sync();
             issue_qk(h, sk);
-            if (h == NH - 1) tc::mma_commit(&bars->kv_empty[sk]);
+            if (h == NH - 1) tc::mma_commit_w(&bars->kv_empty[sk]);
           }
         }
       }
       if (!ok) {
         // wait (bounded) for the MMAs already issued before TMEM is freed
-        tc::mma_commit(&bars->q_full);
+        tc::mma_commit_w(&bars->q_full);
         tc::mbar_wait(&bars->q_full, 1, nullptr, 100000000ull);
       }
     }
