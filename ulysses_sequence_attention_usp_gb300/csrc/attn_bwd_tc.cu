@@ -35,10 +35,15 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 constexpr int BT = 128;                       // rows per tile (queries and keys)
+// Twelve warps: 0 producer, 1 TMEM owner + MMA issuer, 2-3 idle, 4-11
+// elementwise (warp % 4 is the TMEM lane quarter a warp may access).
+constexpr int kThreads = 384;
+constexpr int kEw0 = 4;                       // first elementwise warp
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory plan: NFIX stationary tiles, a ring of NS streamed tiles
-// (two per iteration), barriers, and (VEC) 128 fp32 staged next to each
+// in NS/2 stages of two (one stage per iteration, one full and one empty
+// barrier per stage), barriers, and (VEC) 128 fp32 staged next to each
 // ring slot.
 template <int D, int NFIX, int NS, bool VEC>
 struct CfgT {
@@ -46,6 +51,8 @@ struct CfgT {
   static constexpr int BOX = 128 * 128;
   static constexpr int TILE = NB * BOX;
   static constexpr int NSTAGE = NS;
+  static constexpr int NST2 = NS / 2;        // stages
+  static_assert(NS % 2 == 0, "two tiles per stage");
   static constexpr int FIX_OFF = 0;
   static constexpr int RING_OFF = NFIX * TILE;
   static constexpr int BAR_OFF = RING_OFF + NSTAGE * TILE;
@@ -59,8 +66,8 @@ template <int D> using CfgQ = CfgT<D, 1, 6, false>;
 
 struct Bars {
   uint64_t fix_full;
-  uint64_t ring_full[8];
-  uint64_t ring_empty[8];
+  uint64_t ring_full[4];   // per stage: both tiles (and vectors) landed
+  uint64_t ring_empty[4];  // per stage: the MMAs reading it completed
   uint64_t sd_full;       // dq: S and dP of the iteration computed; dkdv: S^T computed
   uint64_t dp_full;       // dkdv: dP^T computed
   uint64_t consumed;      // dq: both elementwise groups read S and dP (256 arrivals)
@@ -105,9 +112,9 @@ __device__ __forceinline__ int64_t doc_end_of(const Params& p, int64_t t) {
 template <class C>
 __device__ __forceinline__ void init_common(Bars* bars) {
   tc::mbar_init(&bars->fix_full, 1);
-  for (int s = 0; s < C::NSTAGE; ++s) {
-    tc::mbar_init(&bars->ring_full[s], 1);
-    tc::mbar_init(&bars->ring_empty[s], 1);
+  for (int st = 0; st < C::NST2; ++st) {
+    tc::mbar_init(&bars->ring_full[st], 1);
+    tc::mbar_init(&bars->ring_empty[st], 1);
   }
   tc::mbar_init(&bars->sd_full, 1);
   tc::mbar_init(&bars->dp_full, 1);
@@ -123,10 +130,11 @@ __device__ __forceinline__ void init_common(Bars* bars) {
 }
 
 // Producer: two stationary tiles (fixed coordinates) then `n_it` iterations
-// of two streamed tiles each through the ring.  coord(it, w, c0, c1) gives
-// the coordinates of streamed tile w of iteration it (map m0 or m1).  With
-// VEC, vec(it, w) also names 128 fp32 values copied next to the tile (into
-// the slot's vector area; 512 bytes, 16-byte aligned).
+// of two streamed tiles each, one ring stage per iteration (slots 2st and
+// 2st+1).  coord(it, w, c0, c1) gives the coordinates of streamed tile w of
+// iteration it (map m0 or m1).  With VEC, vec(it, w) also names 128 fp32
+// values copied next to the tile (into the slot's vector area; 512 bytes,
+// 16-byte aligned).
 template <class C, bool VEC, typename CoordFn, typename VecFn>
 __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int* abort,
                                         const CUtensorMap* f0, int f0c0, const CUtensorMap* f1,
@@ -144,25 +152,24 @@ __device__ __forceinline__ void produce(uint8_t* smem, Bars* bars, volatile int*
   }
   int issued = 0;
   for (int it = 0; it < n_it && !*abort; ++it) {
+    const int st = it % C::NST2, use = it / C::NST2;
+    if (use > 0 && !tc::mbar_wait(&bars->ring_empty[st], (use - 1) & 1, abort)) break;
+    tc::mbar_expect_tx(&bars->ring_full[st], 2 * (C::TILE + (VEC ? BT * 4 : 0)));
     for (int w = 0; w < 2; ++w) {
-      const int idx = 2 * it + w;
-      const int s = idx % C::NSTAGE, use = idx / C::NSTAGE;
-      if (use > 0 && !tc::mbar_wait(&bars->ring_empty[s], (use - 1) & 1, abort)) break;
+      const int s = 2 * st + w;
       int c0, c1;
       coord(it, w, c0, c1);
-      tc::mbar_expect_tx(&bars->ring_full[s], C::TILE + (VEC ? BT * 4 : 0));
       for (int b = 0; b < C::NB; ++b)
         tc::tma_load_3d(smem + C::RING_OFF + s * C::TILE + b * C::BOX, w == 0 ? m0 : m1,
-                        &bars->ring_full[s], c0 + b * 64, c1, g);
+                        &bars->ring_full[st], c0 + b * 64, c1, g);
       if (VEC)
-        tc::bulk_load(smem + C::VEC_OFF + s * BT * 4, vec(it, w), BT * 4, &bars->ring_full[s]);
-      ++issued;
+        tc::bulk_load(smem + C::VEC_OFF + s * BT * 4, vec(it, w), BT * 4, &bars->ring_full[st]);
     }
+    ++issued;
   }
   if (*abort) {
-    for (int idx = (issued > C::NSTAGE ? issued - C::NSTAGE : 0); idx < issued; ++idx)
-      tc::mbar_wait(&bars->ring_full[idx % C::NSTAGE], (idx / C::NSTAGE) & 1, nullptr,
-                    100000000ull);
+    for (int it = (issued > C::NST2 ? issued - C::NST2 : 0); it < issued; ++it)
+      tc::mbar_wait(&bars->ring_full[it % C::NST2], (it / C::NST2) & 1, nullptr, 100000000ull);
   }
 }
 
@@ -198,8 +205,7 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
   bool ok = tc::mbar_wait_warp(&bars->fix_full, 0, abort) &&
-            tc::mbar_wait_warp(&bars->ring_full[0], 0, abort) &&
-            tc::mbar_wait_warp(&bars->ring_full[1], 0, abort);
+            tc::mbar_wait_warp(&bars->ring_full[0], 0, abort);
   if (ok) {
     tc::fence_after_sync();
     mma_tile_ss<C>(tmem + T0, fix, ring);
@@ -208,8 +214,8 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
     tc::mma_commit_w(&bars->dp_full);
   }
   for (int it = 0; ok && it < n_it; ++it) {
-    const int s0 = (2 * it) % C::NSTAGE, s1 = (2 * it + 1) % C::NSTAGE;
-    const int n0 = (2 * it + 2) % C::NSTAGE, n1 = (2 * it + 3) % C::NSTAGE;
+    const int st = it % C::NST2, nst = (it + 1) % C::NST2;
+    const int s0 = 2 * st, s1 = 2 * st + 1, n0 = 2 * nst, n1 = 2 * nst + 1;
     const bool more = it + 1 < n_it;
     // dV(it) += P^T(it) dO(it)
     if (!(ok = tc::mbar_wait_warp(&bars->p_full[0], it & 1, abort))) break;
@@ -222,7 +228,7 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
     tc::mma_commit_w(&bars->done[0]);
     // S^T(it+1) once dV(it) has read P^T(it)
     if (more) {
-      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n0], ((2 * it + 2) / C::NSTAGE) & 1, abort))) break;
+      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[nst], ((it + 1) / C::NST2) & 1, abort))) break;
       if (!(ok = tc::mbar_wait_warp(&bars->done[0], it & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_ss<C>(tmem + T0, fix, ring + n0 * C::TILE);
@@ -237,11 +243,9 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
                  tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
     tc::mma_commit_w(&bars->done[1]);
-    tc::mma_commit_w(&bars->ring_empty[s0]);
-    tc::mma_commit_w(&bars->ring_empty[s1]);
+    tc::mma_commit_w(&bars->ring_empty[st]);
     // dP^T(it+1) once dK(it) has read dS^T(it)
     if (more) {
-      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n1], ((2 * it + 3) / C::NSTAGE) & 1, abort))) break;
       if (!(ok = tc::mbar_wait_warp(&bars->done[1], it & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_ss<C>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
@@ -284,27 +288,23 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
   bool ok = tc::mbar_wait_warp(&bars->fix_full, 0, abort) &&
             tc::mbar_wait_warp(&bars->q_ready, 0, abort) &&
-            tc::mbar_wait_warp(&bars->ring_full[0], 0, abort) &&
-            tc::mbar_wait_warp(&bars->ring_full[1], 0, abort);
+            tc::mbar_wait_warp(&bars->ring_full[0], 0, abort);
   if (ok) {
     tc::fence_after_sync();
     mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring);
     mma_tile_ss<C>(tmem + T1, fix, ring + C::TILE);
     tc::mma_commit_w(&bars->sd_full);
-    tc::mma_commit_w(&bars->ring_empty[1]);      // V_0 is only read by dP(0)
   }
   for (int j = 0; ok && j < n_it; ++j) {
-    const int s0 = (2 * j) % C::NSTAGE, s1 = (2 * j + 1) % C::NSTAGE;
+    const int st = j % C::NST2, s0 = 2 * st;
     if (!(ok = tc::mbar_wait_warp(&bars->consumed, j & 1, abort))) break;
     if (j + 1 < n_it) {
-      const int n0 = (2 * j + 2) % C::NSTAGE, n1 = (2 * j + 3) % C::NSTAGE;
-      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n0], ((2 * j + 2) / C::NSTAGE) & 1, abort))) break;
-      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[n1], ((2 * j + 3) / C::NSTAGE) & 1, abort))) break;
+      const int nst = (j + 1) % C::NST2, n0 = 2 * nst, n1 = 2 * nst + 1;
+      if (!(ok = tc::mbar_wait_warp(&bars->ring_full[nst], ((j + 1) / C::NST2) & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring + n0 * C::TILE);
       mma_tile_ss<C>(tmem + T1, fix, ring + n1 * C::TILE);
       tc::mma_commit_w(&bars->sd_full);
-      tc::mma_commit_w(&bars->ring_empty[n1]);   // V_{j+1} is only read by dP(j+1)
     }
     if (!(ok = tc::mbar_wait_warp(&bars->p_full[0], j & 1, abort))) break;
     tc::fence_after_sync();
@@ -314,8 +314,7 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
                  tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (j > 0 || kk > 0) ? 1u : 0u);
     tc::mma_commit_w(&bars->done[0]);
-    tc::mma_commit_w(&bars->ring_empty[s0]);     // K_j: read by S(j) and dQ(j)
-    (void)s1;                                   // V_j was released after dP(j)
+    tc::mma_commit_w(&bars->ring_empty[st]);     // K_j (S(j), dQ(j)) and V_j (dP(j))
   }
   if (!ok) {
     tc::mma_commit_w(&bars->drain);
@@ -326,59 +325,70 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
 // dK/dV elementwise work on half h (queries [64h, 64h+64)) of this thread's
 // key row, in two phases so that each overlaps an MMA:
 //   phase 1 (while dP^T is computed): P^T = exp2(S^T*sl2 - lse2[col]),
-//            written as bf16 over S^T, kept in fp32 registers;
+//            written as bf16 over S^T and kept, as the same bf16 pairs, in
+//            32 registers;
 //   phase 2 (while dV is computed):   dS^T = P^T (dP^T - delta[col]),
 //            written as bf16 over dP^T.
+// dS^T is thus formed from the bf16 P^T that dV is built from (a relative
+// change of at most 2^-9 per element, the size of the rounding dS^T gets
+// anyway).  The per-column lse2 and delta come in registers.
 // bf16 values of each 32-column chunk go to that chunk's first 16 columns.
 // Columns outside [lo, hi] are zero when MASK.
 template <bool MASK>
 __device__ __forceinline__ void dkdv_phase_p(uint32_t tS, int h, int lo, int hi,
-                                             const float* lse2, float sl2, float (&pf)[64]) {
-  uint32_t sv[64];
-  tc::tmem_ld_x64(tS + 64 * h, sv);
+                                             const float (&l2)[64], float sl2, uint32_t (&pk)[32]) {
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
+  for (int cc = 0; cc < 2; ++cc) {   // two 32-column chunks (fewer live registers)
+    uint32_t sv[32];
+    tc::tmem_ld_x32(tS + 64 * h + 32 * cc, sv);
     uint32_t pw[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {   // shared memory, same address in every lane
-      const float4 a = reinterpret_cast<const float4*>(lse2 + 64 * h + 32 * cc)[i];
-      const float l2[4] = {a.x, a.y, a.z, a.w};
+    for (int i = 0; i < 16; ++i) {
+      float pv[2];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int k = 32 * cc + 4 * i + e;
-        float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -l2[e]));
+      for (int e = 0; e < 2; ++e) {
+        const int k = 32 * cc + 2 * i + e;
+        pv[e] = tc::ex2(fmaf(__uint_as_float(sv[2 * i + e]), sl2, -l2[k]));
         if (MASK) {
           const int col = 64 * h + k;
-          if (!(col >= lo && col <= hi)) pv = 0.f;
+          if (!(col >= lo && col <= hi)) pv[e] = 0.f;
         }
-        pf[k] = pv;
       }
-      pw[2 * i] = tc::pack_bf16(pf[32 * cc + 4 * i], pf[32 * cc + 4 * i + 1]);
-      pw[2 * i + 1] = tc::pack_bf16(pf[32 * cc + 4 * i + 2], pf[32 * cc + 4 * i + 3]);
+      pw[i] = tc::pack_bf16(pv[0], pv[1]);
+      pk[16 * cc + i] = pw[i];
     }
     tc::tmem_st_x16(tS + 64 * h + 32 * cc, pw);
   }
 }
 
-__device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, int h, const float* dl,
-                                              const float (&pf)[64]) {
+__device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, int h, const float (&d2)[64],
+                                              const uint32_t (&pk)[32]) {
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     uint32_t dv[32];
     tc::tmem_ld_x32(tP + 64 * h + 32 * cc, dv);
     uint32_t dw[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float4 b = reinterpret_cast<const float4*>(dl + 64 * h + 32 * cc)[i];
-      const float d2[4] = {b.x, b.y, b.z, b.w};
-      float dd[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        dd[e] = pf[32 * cc + 4 * i + e] * (__uint_as_float(dv[4 * i + e]) - d2[e]);
-      dw[2 * i] = tc::pack_bf16(dd[0], dd[1]);
-      dw[2 * i + 1] = tc::pack_bf16(dd[2], dd[3]);
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t w = pk[16 * cc + i];
+      const float p0 = __uint_as_float(w << 16), p1 = __uint_as_float(w & 0xffff0000u);
+      const int k = 32 * cc + 2 * i;
+      dw[i] = tc::pack_bf16(p0 * (__uint_as_float(dv[2 * i]) - d2[k]),
+                            p1 * (__uint_as_float(dv[2 * i + 1]) - d2[k + 1]));
     }
     tc::tmem_st_x16(tP + 64 * h + 32 * cc, dw);
+  }
+}
+
+// 64 fp32 values from shared memory (the same address in every lane) into
+// registers.  The loads are issued early, where the warp would wait anyway:
+// while the SS MMAs stream their operands, a shared-memory load issued in
+// the middle of an elementwise phase waits a long time for its turn.
+__device__ __forceinline__ void load_vec64(const float* src, float (&v)[64]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float4 a = reinterpret_cast<const float4*>(src)[i];
+    v[4 * i] = a.x; v[4 * i + 1] = a.y; v[4 * i + 2] = a.z; v[4 * i + 3] = a.w;
   }
 }
 
@@ -433,7 +443,7 @@ __device__ __forceinline__ void store_row32(bf16* dst, const uint32_t (&v)[32], 
 
 // ------------------------------------------------------------------- dK, dV
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const Params p) {
@@ -491,43 +501,55 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     if (n_it > 0) mma_loop_dkdv<D>(smem, bars, abort, tmem, n_it);   // whole warp
-  } else if (warp >= 4) {
+  } else if (warp >= kEw0) {
     const int quarter = warp & 3;
-    const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)
+    const int half = (warp - kEw0) >> 2;       // columns [64*half, 64*half + 64)
     const int r = quarter * 32 + lane;
     const int64_t u = u0 + r;
     const int64_t de = doc_end_of(p, u);         // queries [u, de) see key u
     const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
     const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
+    // per-query LSE*log2(e) (next to the Q tile) and delta (next to the dO
+    // tile) of this half's 64 columns, staged by the producer
+    const float* vec = reinterpret_cast<const float*>(smem + C::VEC_OFF) + 64 * half;
+    float l2[64];
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
+    if (n_it > 0) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->ring_full[0], 0, abort));
+      if (ok) load_vec64(vec, l2);
+    }
+    for (int it = 0; ok && it < n_it; ++it) {
       const int64_t t0 = tq0 + (int64_t)(it / p.G) * BT;
-      const int s0 = (2 * it) % C::NSTAGE, s1 = (2 * it + 1) % C::NSTAGE;
-      ok = __all_sync(0xffffffffu,
-                      tc::mbar_wait(&bars->sd_full, it & 1, abort) &&
-                          tc::mbar_wait(&bars->ring_full[s0], ((2 * it) / C::NSTAGE) & 1, abort) &&
-                          tc::mbar_wait(&bars->ring_full[s1], ((2 * it + 1) / C::NSTAGE) & 1, abort));
+      const int s1 = 2 * (it % C::NST2) + 1;     // this stage's dO slot (delta)
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full, it & 1, abort));
       if (!ok) break;
       tc::fence_after_sync();
-      // per-query LSE*log2(e) and delta of this tile, staged by the producer
-      const float* lse2 = reinterpret_cast<const float*>(smem + C::VEC_OFF + s0 * BT * 4);
-      const float* dl = reinterpret_cast<const float*>(smem + C::VEC_OFF + s1 * BT * 4);
       const int lo = (int)max((int64_t)0, min((int64_t)BT, u - t0));
       const int hi = de < 0 ? -1 : (int)min((int64_t)BT - 1, de - 1 - t0);
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
-      float pf[64];
-      if (mask) dkdv_phase_p<true>(tS, half, lo, hi, lse2, p.scale_log2, pf);
-      else dkdv_phase_p<false>(tS, half, lo, hi, lse2, p.scale_log2, pf);
+      uint32_t pk[32];
+      if (mask) dkdv_phase_p<true>(tS, half, lo, hi, l2, p.scale_log2, pk);
+      else dkdv_phase_p<false>(tS, half, lo, hi, l2, p.scale_log2, pk);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bars->p_full[0]);
+      float d2[64];
+      load_vec64(vec + s1 * BT, d2);
       ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->dp_full, it & 1, abort));
       if (!ok) break;
       tc::fence_after_sync();
-      dkdv_phase_ds(tP, half, dl, pf);
+      dkdv_phase_ds(tP, half, d2, pk);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bars->p_full[1]);
+      // the next iteration's lse2, loaded while the S^T MMA runs (after the
+      // last iteration the loads read a slot's stale values, never used: an
+      // unconditional load keeps the old values from living through phase 2)
+      const int nst = (it + 1) % C::NST2;
+      if (it + 1 < n_it)
+        ok = __all_sync(0xffffffffu,
+                        tc::mbar_wait(&bars->ring_full[nst], ((it + 1) / C::NST2) & 1, abort));
+      load_vec64(vec + 2 * nst * BT, l2);
     }
     if (ok && n_it > 0) {   // dK is the last MMA; it completes after dV
       ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[1], (n_it - 1) & 1, abort));
@@ -562,7 +584,7 @@ __global__ void __launch_bounds__(384, 1)
 
 // ----------------------------------------------------------------------- dQ
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
               const Params p) {
@@ -613,9 +635,9 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     if (n_kv > 0) mma_loop_dq<D>(smem, bars, abort, tmem, n_kv);     // whole warp
-  } else if (warp >= 4) {
+  } else if (warp >= kEw0) {
     const int quarter = warp & 3;
-    const int half = (warp - 4) >> 2;          // columns [64*half, 64*half + 64)
+    const int half = (warp - kEw0) >> 2;       // columns [64*half, 64*half + 64)
     const int r = quarter * 32 + lane;
     const int64_t t = t0 + r;
     const int64_t ds = doc_start_of(p, t);
@@ -767,10 +789,10 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
   if ((e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem_q)) != cudaSuccess)
     return e;
-  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), 384, smem_kv, st>>>(
+  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), kThreads, smem_kv, st>>>(
       mq, mk, mv, mdo, prm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), 384, smem_q, st>>>(
+  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), kThreads, smem_q, st>>>(
       mq, mk, mv, mdo, prm);
   usp_count_launches(3);
   return cudaGetLastError();
