@@ -76,7 +76,7 @@ struct Bars {
                           // dq: dS written ([0]); 256 arrivals each
   uint64_t done[2];       // dkdv: dV MMA done ([0]), dK MMA done ([1]);
                           // dq: dQ MMA that read dS done ([0])
-  uint64_t drain;
+  uint64_t drain;         // wind-down: the MMAs issued so far completed
   uint32_t tmem_base;
   int abort;
 };
@@ -109,12 +109,14 @@ __device__ __forceinline__ int64_t doc_end_of(const Params& p, int64_t t) {
   return p.cu ? (int64_t)__ldg(p.cu + d + 1) : p.S;
 }
 
+// empty_count: commits that release a ring stage (one per issuing warp that
+// reads it).
 template <class C>
-__device__ __forceinline__ void init_common(Bars* bars) {
+__device__ __forceinline__ void init_common(Bars* bars, int empty_count) {
   tc::mbar_init(&bars->fix_full, 1);
   for (int st = 0; st < C::NST2; ++st) {
     tc::mbar_init(&bars->ring_full[st], 1);
-    tc::mbar_init(&bars->ring_empty[st], 1);
+    tc::mbar_init(&bars->ring_empty[st], empty_count);
   }
   tc::mbar_init(&bars->sd_full, 1);
   tc::mbar_init(&bars->dp_full, 1);
@@ -260,13 +262,15 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
 
 // dQ MMA issuer.  The Q tile of this CTA sits in TMEM (columns QC..QC+63,
 // written once by the elementwise groups), so S needs no shared-memory
-// reads for its A operand.  Iteration j streams key tile K_j (R0), V_j (R1):
+// reads for its A operand.  Iteration j streams key tile K_j and V_j (one
+// ring stage):
 //   S(j) = Q K_j^T (T0, TS),  dP(j) = dO V_j^T (T1, SS)
 //   dQ += dS(j) K_j   with dS(j) in TMEM columns R..R+63              (TS)
 // S(j+1) and dP(j+1) are issued as soon as the elementwise groups have read
 // S(j) and dP(j) ("consumed"), before they finish dS(j), so the tensor pipe
 // keeps working while they compute.  The dS columns are rewritten for j+1
-// only after done[0] of dQ(j).
+// only after done[0] of dQ(j).  (Issuing dQ from a second warp was slower:
+// the two streams interleave their MMAs in the pipe.)
 template <int D>
 __device__ __forceinline__ void mma_tile_s_ts(uint32_t d_tmem, uint32_t q_tmem, uint32_t k) {
   using C = CfgQ<D>;
@@ -278,11 +282,13 @@ __device__ __forceinline__ void mma_tile_s_ts(uint32_t d_tmem, uint32_t q_tmem, 
   }
 }
 
+// dQ kernel TMEM columns: S, dP, the dQ accumulator, dS (bf16), Q (bf16)
+constexpr uint32_t kDqT0 = 0, kDqT1 = 128, kDqAcc = 256, kDqR = 384, kDqQ = 448;
+
 template <int D>
 __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile int* abort,
                                             uint32_t tmem, int n_it) {
   using C = CfgQ<D>;
-  constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, R = 384, QC = 448;
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
@@ -291,8 +297,8 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
             tc::mbar_wait_warp(&bars->ring_full[0], 0, abort);
   if (ok) {
     tc::fence_after_sync();
-    mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring);
-    mma_tile_ss<C>(tmem + T1, fix, ring + C::TILE);
+    mma_tile_s_ts<D>(tmem + kDqT0, tmem + kDqQ, ring);
+    mma_tile_ss<C>(tmem + kDqT1, fix, ring + C::TILE);
     tc::mma_commit_w(&bars->sd_full);
   }
   for (int j = 0; ok && j < n_it; ++j) {
@@ -302,17 +308,17 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
       const int nst = (j + 1) % C::NST2, n0 = 2 * nst, n1 = 2 * nst + 1;
       if (!(ok = tc::mbar_wait_warp(&bars->ring_full[nst], ((j + 1) / C::NST2) & 1, abort))) break;
       tc::fence_after_sync();
-      mma_tile_s_ts<D>(tmem + T0, tmem + QC, ring + n0 * C::TILE);
-      mma_tile_ss<C>(tmem + T1, fix, ring + n1 * C::TILE);
+      mma_tile_s_ts<D>(tmem + kDqT0, tmem + kDqQ, ring + n0 * C::TILE);
+      mma_tile_ss<C>(tmem + kDqT1, fix, ring + n1 * C::TILE);
       tc::mma_commit_w(&bars->sd_full);
     }
     if (!(ok = tc::mbar_wait_warp(&bars->p_full[0], j & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-      tc::mma_ts_w(tmem + A0, tmem + R + 8 * kk,
-                 tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+      tc::mma_ts_w(tmem + kDqAcc, tmem + kDqR + 8 * kk,
+                   tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
+                   (j > 0 || kk > 0) ? 1u : 0u);
     tc::mma_commit_w(&bars->done[0]);
     tc::mma_commit_w(&bars->ring_empty[st]);     // K_j (S(j), dQ(j)) and V_j (dP(j))
   }
@@ -471,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int n_it = n_q * p.G;    // iteration it: query tile it / G, head jk*G + it % G
 
-  if (threadIdx.x == 0) init_common<C>(bars);
+  if (threadIdx.x == 0) init_common<C>(bars, 1);
   if (warp == 1) {
     tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
@@ -611,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (threadIdx.x == 0) init_common<C>(bars);
+  if (threadIdx.x == 0) init_common<C>(bars, 1);
   if (warp == 1) {
     tc::tmem_alloc(&bars->tmem_base, 512);
     tc::tmem_relinquish();
@@ -647,8 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       lse2 = __ldg(p.lse2 + li);
       dl = __ldg(p.delta + li);
     }
-    const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
-    const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
+    const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, kDqT0);
+    const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, kDqT1);
     bool ok = true;
     // this thread's Q row, columns [64*half, 64*half + 64), into TMEM as
     // the A operand of S = Q K^T (bf16 pairs, 32 columns)
@@ -662,12 +668,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint4 v = (t < p.S_pad && mine) ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
         qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
       }
-      if (D == 128 || half == 0) tc::tmem_st_x32(tc::tmem_addr(tmem, quarter * 32, 448 + 32 * half), qw);
+      if (D == 128 || half == 0)
+        tc::tmem_st_x32(tc::tmem_addr(tmem, quarter * 32, kDqQ + 32 * half), qw);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bars->q_ready);
     }
-    const uint32_t tR = tc::tmem_addr(tmem, quarter * 32, 384);
+    const uint32_t tR = tc::tmem_addr(tmem, quarter * 32, kDqR);
     for (int it = 0; it < n_kv; ++it) {
       ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full, it & 1, abort));
       if (!ok) break;
@@ -694,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
       uint32_t v[32];
       if (have) {
-        tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, 256 + c * 32), v);
+        tc::tmem_ld_x32(tc::tmem_addr(tmem, quarter * 32, kDqAcc + c * 32), v);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
