@@ -428,7 +428,7 @@ __device__ __forceinline__ bool dq_half(uint32_t tS, uint32_t tP, uint32_t tR, i
     w[i] = tc::pack_bf16(dd[0], dd[1]);
   }
   if (j >= 1) {   // the dQ MMA of iteration j-1 read the dS columns
-    if (!__all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], (j - 1) & 1, abort)))
+    if (!tc::mbar_wait_warp(&bars->done[0], (j - 1) & 1, abort))
       return false;
     tc::fence_after_sync();
   }
@@ -521,13 +521,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l2[64];
     bool ok = true;
     if (n_it > 0) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->ring_full[0], 0, abort));
+      ok = tc::mbar_wait_warp(&bars->ring_full[0], 0, abort);
       if (ok) load_vec64(vec, l2);
     }
     for (int it = 0; ok && it < n_it; ++it) {
       const int64_t t0 = tq0 + (int64_t)(it / p.G) * BT;
       const int s1 = 2 * (it % C::NST2) + 1;     // this stage's dO slot (delta)
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full, it & 1, abort));
+      ok = tc::mbar_wait_warp(&bars->sd_full, it & 1, abort);
       if (!ok) break;
       tc::fence_after_sync();
       const int lo = (int)max((int64_t)0, min((int64_t)BT, u - t0));
@@ -541,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(&bars->p_full[0]);
       float d2[64];
       load_vec64(vec + s1 * BT, d2);
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->dp_full, it & 1, abort));
+      ok = tc::mbar_wait_warp(&bars->dp_full, it & 1, abort);
       if (!ok) break;
       tc::fence_after_sync();
       dkdv_phase_ds(tP, half, d2, pk);
@@ -553,12 +553,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // unconditional load keeps the old values from living through phase 2)
       const int nst = (it + 1) % C::NST2;
       if (it + 1 < n_it)
-        ok = __all_sync(0xffffffffu,
-                        tc::mbar_wait(&bars->ring_full[nst], ((it + 1) / C::NST2) & 1, abort));
+        ok = tc::mbar_wait_warp(&bars->ring_full[nst], ((it + 1) / C::NST2) & 1, abort);
       load_vec64(vec + 2 * nst * BT, l2);
     }
     if (ok && n_it > 0) {   // dK is the last MMA; it completes after dV
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[1], (n_it - 1) & 1, abort));
+      ok = tc::mbar_wait_warp(&bars->done[1], (n_it - 1) & 1, abort);
       tc::fence_after_sync();
     }
     // epilogue: the left half writes dV, the right half dK
@@ -676,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t tR = tc::tmem_addr(tmem, quarter * 32, kDqR);
     for (int it = 0; it < n_kv; ++it) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->sd_full, it & 1, abort));
+      ok = tc::mbar_wait_warp(&bars->sd_full, it & 1, abort);
       if (!ok) break;
       tc::fence_after_sync();
       const int64_t u0 = kv_start + (int64_t)it * BT;
@@ -692,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::mbar_arrive(&bars->p_full[0]);
     }
     if (ok && n_kv > 0) {   // the last dQ MMA completes after all earlier ones
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->done[0], (n_kv - 1) & 1, abort));
+      ok = tc::mbar_wait_warp(&bars->done[0], (n_kv - 1) & 1, abort);
       tc::fence_after_sync();
     }
     const bool have = ok && n_kv > 0;

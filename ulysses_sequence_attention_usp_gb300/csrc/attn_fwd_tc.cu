@@ -293,7 +293,7 @@ __global__ void __launch_bounds__(384, 1)
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int jt = 0; jt < n_kv; ++jt) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->s_full[h], jt & 1, abort));
+        ok = tc::mbar_wait_warp(&bars->s_full[h], jt & 1, abort);
         if (!ok) break;
         tc::fence_after_sync();
         const int64_t u0 = kv_start + (int64_t)jt * BN;
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(384, 1)
         l = l * alpha + rowsum;
         m = m_use;
         if (jt > 0 && __any_sync(0xffffffffu, rescale)) {
-          ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->o_full[h], (jt - 1) & 1, abort));
+          ok = tc::mbar_wait_warp(&bars->o_full[h], (jt - 1) & 1, abort);
           if (!ok) break;
           tc::fence_after_sync();
 #pragma unroll
@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       // ---- epilogue: O = O / l, LSE = ln(sum)
       if (ok && n_kv > 0) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(&bars->o_full[h], (n_kv - 1) & 1, abort));
+        ok = tc::mbar_wait_warp(&bars->o_full[h], (n_kv - 1) & 1, abort);
         tc::fence_after_sync();
       }
       const bool has = ok && l > 0.f;

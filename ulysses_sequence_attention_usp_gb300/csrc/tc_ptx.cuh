@@ -271,9 +271,14 @@ __device__ __forceinline__ void mma_commit_w(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
-// Bounded wait by a whole warp; the result is the same in every lane.
+// Bounded wait by a whole warp; the result is the same in every lane.  The
+// common case, a phase that has already completed, takes a straight-line
+// path (one try_wait and a vote, ~20 cycles); entering the bounded loop and
+// reconverging after it costs ~100 cycles more, which the MMA-issuing warp
+// cannot afford between MMA groups.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
                                                volatile int* abort) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort));
 }
 
