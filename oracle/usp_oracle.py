@@ -248,25 +248,33 @@ def rope_recipe_bf16(x_bits: np.ndarray, pos: np.ndarray, table: np.ndarray,
 # Accuracy Test: parity with full-sequence attention).  Causal GQA with a
 # per-document mask: key u is visible to query t iff doc(u) == doc(t) >= 0
 # and u <= t.  Q head h reads KV head h // (Hq/Hkv).
+#
+# causal=False is the bidirectional variant (zhtmike/verl PR #45 "[trainer]
+# feat: support sequence parallel", What does this PR do: Ulysses SP for the
+# Diffusers SDPA attention, whose attention mask masks the padding added for
+# SP alignment): key u is visible to query t iff doc(u) == doc(t) >= 0, so
+# pad rows (doc -1) are never keys and every row of a document sees the
+# whole document.
 # ---------------------------------------------------------------------------
 
 _ROW_CHUNK = 2048  # rows are evaluated in independent chunks to bound memory
 
 
-def _visible(rows: np.ndarray, doc: np.ndarray) -> np.ndarray:
+def _visible(rows: np.ndarray, doc: np.ndarray, causal: bool = True) -> np.ndarray:
     u = np.arange(doc.shape[0])
     dr = doc[rows][:, None]
-    return (dr >= 0) & (doc[None, :] == dr) & (u[None, :] <= rows[:, None])
+    vis = (dr >= 0) & (doc[None, :] == dr)
+    return vis & (u[None, :] <= rows[:, None]) if causal else vis
 
 
 def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, doc: np.ndarray,
-                   rows: np.ndarray, scale: float):
+                   rows: np.ndarray, scale: float, causal: bool = True):
     """Softmax attention of single-head fp64 q[T,D], k, v for the query rows
     ``rows``.  Returns O[len(rows), D] and LSE[len(rows)] (natural log; -inf
     and O=0 for a row with no visible key)."""
     rows = np.asarray(rows, dtype=np.int64)
     s = (q[rows] @ k.T) * scale
-    vis = _visible(rows, doc)
+    vis = _visible(rows, doc, causal)
     s = np.where(vis, s, -np.inf)
     m = s.max(axis=1)
     has = np.isfinite(m)
@@ -280,7 +288,7 @@ def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, doc: np.ndarray,
 
 
 def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, doc: np.ndarray,
-                  scale: float):
+                  scale: float, causal: bool = True):
     """q[T][Hq][D], k/v[T][Hkv][D] (fp64) -> O[T][Hq][D], LSE[Hq][T]."""
     T, Hq, D = q.shape
     G = Hq // k.shape[1]
@@ -290,11 +298,11 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, doc: np.ndarray,
         for a in range(0, T, _ROW_CHUNK):
             rows = np.arange(a, min(T, a + _ROW_CHUNK))
             o[rows, h], lse[h, rows] = attention_rows(q[:, h], k[:, h // G],
-                                                      v[:, h // G], doc, rows, scale)
+                                                      v[:, h // G], doc, rows, scale, causal)
     return o, lse
 
 
-def attention_bwd_head(q, k, v, do, doc, scale, rows=None):
+def attention_bwd_head(q, k, v, do, doc, scale, rows=None, causal=True):
     """Gradients of L = sum(O * dO) for one head (fp64, q/k/v/do [T][D]).
 
     With P = softmax rows:  dV = P^T dO;  dP = dO V^T;
@@ -310,7 +318,7 @@ def attention_bwd_head(q, k, v, do, doc, scale, rows=None):
     for a in range(0, rows_all.shape[0], _ROW_CHUNK):
         rows = rows_all[a:a + _ROW_CHUNK]
         s = (q[rows] @ k.T) * scale
-        vis = _visible(rows, doc)
+        vis = _visible(rows, doc, causal)
         s = np.where(vis, s, -np.inf)
         m = s.max(axis=1)
         has = np.isfinite(m)
@@ -326,7 +334,7 @@ def attention_bwd_head(q, k, v, do, doc, scale, rows=None):
     return dq, dk, dv
 
 
-def attention_bwd(q, k, v, do, doc, scale):
+def attention_bwd(q, k, v, do, doc, scale, causal=True):
     """All heads: q/do[T][Hq][D], k/v[T][Hkv][D] -> dq, dk, dv (fp64).  dK and
     dV of a KV head are summed over the Hq/Hkv query heads that read it."""
     T, Hq, D = q.shape
@@ -337,7 +345,7 @@ def attention_bwd(q, k, v, do, doc, scale):
     dv = np.zeros((T, Hkv, D))
     for h in range(Hq):
         a, b, c = attention_bwd_head(q[:, h], k[:, h // G], v[:, h // G], do[:, h],
-                                     doc, scale)
+                                     doc, scale, causal=causal)
         dq[:, h] = a
         dk[:, h // G] += b
         dv[:, h // G] += c
@@ -355,20 +363,20 @@ def default_scale(D: int) -> float:
     return 1.0 / math.sqrt(D)
 
 
-def full_sequence(q, k, v, do, cu, cos, sin, scale):
+def full_sequence(q, k, v, do, cu, cos, sin, scale, causal=True):
     """Reference computation on the unsharded sequence (fp64 inputs [S][H][D])."""
     S = q.shape[0]
     pos, doc = positions_docs(S, 1, cu)
     qr = rope_rotate(q, pos, cos, sin)
     kr = rope_rotate(k, pos, cos, sin)
-    o, lse = attention_fwd(qr, kr, v, doc, scale)
-    dqr, dkr, dv = attention_bwd(qr, kr, v, do, doc, scale)
+    o, lse = attention_fwd(qr, kr, v, doc, scale, causal)
+    dqr, dkr, dv = attention_bwd(qr, kr, v, do, doc, scale, causal)
     dq = rope_rotate(dqr, pos, cos, sin, inverse=True)
     dk = rope_rotate(dkr, pos, cos, sin, inverse=True)
     return dict(o=o, lse=lse, loss=float((o * do).sum()), dq=dq, dk=dk, dv=dv)
 
 
-def ulysses(q, k, v, do, cu, cos, sin, scale, P):
+def ulysses(q, k, v, do, cu, cos, sin, scale, P, causal=True):
     """The Ulysses path: pad and shard, all-to-all to head groups, RoPE at
     absolute positions, attention per head group, all-to-all back."""
     S, Hq, D = q.shape
@@ -388,8 +396,8 @@ def ulysses(q, k, v, do, cu, cos, sin, scale, P):
         qg = rope_rotate(heads["q"][g], pos, cos, sin)
         kg = rope_rotate(heads["k"][g], pos, cos, sin)
         vg = heads["v"][g]
-        o_h[g], lse_h[g] = attention_fwd(qg, kg, vg, doc, scale)
-        a, b, c = attention_bwd(qg, kg, vg, heads["do"][g], doc, scale)
+        o_h[g], lse_h[g] = attention_fwd(qg, kg, vg, doc, scale, causal)
+        a, b, c = attention_bwd(qg, kg, vg, heads["do"][g], doc, scale, causal)
         dq_h[g] = rope_rotate(a, pos, cos, sin, inverse=True)
         dk_h[g] = rope_rotate(b, pos, cos, sin, inverse=True)
         dv_h[g] = c
