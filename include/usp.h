@@ -61,7 +61,7 @@ typedef enum {
   USP_OK = 0,
   USP_ERR_INVALID_ARG = 1,          /* NULL/misaligned pointer, bad size, bad table */
   USP_ERR_HEADS_NOT_DIVISIBLE = 2,  /* P does not divide Hq or Hkv, or Hkv does not divide Hq */
-  USP_ERR_UNSUPPORTED = 3,          /* e.g. D not in {64,128}, causal != 1 */
+  USP_ERR_UNSUPPORTED = 3,          /* e.g. D not in {64,128} */
   USP_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
   USP_ERR_TIMEOUT = 5               /* a device-side wait gave up (see usp_device_status) */
 } usp_status;
@@ -77,7 +77,11 @@ typedef struct {
                                        it is checked (cu[0]=0, non-decreasing,
                                        cu[n_docs]=S) before launch */
   int32_t n_docs;                   /* documents in cu_seqlens (ignored if NULL) */
-  int32_t causal;                   /* must be 1 (causal within each document) */
+  int32_t causal;                   /* 1: causal within each document; 0:
+                                       bidirectional within each document
+                                       (verl PR #45, Diffusers SDPA under
+                                       Ulysses); anything else is
+                                       USP_ERR_INVALID_ARG */
   float scale;                      /* softmax scale; 0 => 1/sqrt(D) */
 } usp_dims;
 
@@ -130,8 +134,10 @@ usp_status usp_seq_to_head_rope(const usp_dims* dims, const void* x_seq, int32_t
  * h / (Hq/Hkv)) and row t with doc(t) >= 0:
  *   O[t]   = sum_{u in M(t)} softmax_u(scale * q_t . k_u) v_u
  *   LSE[t] = ln sum_{u in M(t)} exp(scale * q_t . k_u)
- *   M(t)   = { u : doc(u) == doc(t), u <= t }.
- * Rows with doc(t) = -1 (padding) get O = 0 and LSE = -inf.
+ *   M(t)   = { u : doc(u) == doc(t), u <= t }         (causal = 1)
+ *   M(t)   = { u : doc(u) == doc(t) }                 (causal = 0)
+ * Rows with doc(t) = -1 (padding) get O = 0 and LSE = -inf, and are never
+ * keys (in the bidirectional case this is the padding mask).
  *   q_h [P][S_pad][Hq/P][D], k_h/v_h [P][S_pad][Hkv/P][D] (bf16, head layout)
  *   doc [S_pad] int32 (from usp_pad_shard)
  *   o_h [P][S_pad][Hq/P][D] bf16 (output), lse [P][Hq/P][S_pad] fp32 (output)

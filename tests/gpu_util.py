@@ -71,8 +71,9 @@ class SampledOracle:
     exact fp64 rotation of the oracle (this is the end-to-end reference).
     """
 
-    def __init__(self, q, k, v, do, cu, wl):
+    def __init__(self, q, k, v, do, cu, wl, causal=True):
         self.wl = wl
+        self.causal = causal
         S, D = wl.S, wl.D
         self.S = S
         self.G = wl.Hq // wl.Hkv
@@ -97,7 +98,7 @@ class SampledOracle:
         qr = np.zeros((self.S, self.wl.D))
         qr[rows] = self._rot(self.q[rows, h], rows)
         return O.attention_rows(qr, self.k_rot(kh), O.bf16_to_f64(self.v[:, kh]), self.doc,
-                                np.asarray(rows), self.scale)
+                                np.asarray(rows), self.scale, self.causal)
 
     def dq_rows(self, h, rows):
         """Pre-RoPE dQ of head h at the given rows."""
@@ -106,14 +107,16 @@ class SampledOracle:
         qr[rows] = self._rot(self.q[rows, h], rows)
         dq, _, _ = O.attention_bwd_head(qr, self.k_rot(kh), O.bf16_to_f64(self.v[:, kh]),
                                         O.bf16_to_f64(self.do[:, h]), self.doc, self.scale,
-                                        rows=np.asarray(rows))
+                                        rows=np.asarray(rows), causal=self.causal)
         return O.rope_rotate(dq[:, None, :], self.pos[rows], self.cos, self.sin,
                              inverse=True)[:, 0]
 
-    def dkv_tail(self, kh, u_lo, u_hi):
+    def dkv_tail(self, kh, u_lo, u_hi, q_lo=None):
         """Pre-RoPE dK and dV of KV head kh at keys [u_lo, u_hi), which must lie
-        in one document that ends at u_hi (so only queries >= u_lo see them)."""
-        rows = np.arange(u_lo, u_hi)
+        in one document that ends at u_hi.  The queries that see them are
+        [u_lo, u_hi) when causal; bidirectional, pass q_lo = the document's
+        first row so that all of its queries contribute."""
+        rows = np.arange(u_lo if q_lo is None else q_lo, u_hi)
         dk = np.zeros((u_hi - u_lo, self.wl.D))
         dv = np.zeros_like(dk)
         for i in range(self.G):
@@ -122,8 +125,9 @@ class SampledOracle:
             qr[rows] = self._rot(self.q[rows, h], rows)
             _, a, b = O.attention_bwd_head(qr, self.k_rot(kh), O.bf16_to_f64(self.v[:, kh]),
                                            O.bf16_to_f64(self.do[:, h]), self.doc, self.scale,
-                                           rows=rows)
+                                           rows=rows, causal=self.causal)
             dk += a[u_lo:u_hi]
             dv += b[u_lo:u_hi]
-        dk = O.rope_rotate(dk[:, None, :], self.pos[rows], self.cos, self.sin, inverse=True)[:, 0]
+        keys = np.arange(u_lo, u_hi)
+        dk = O.rope_rotate(dk[:, None, :], self.pos[keys], self.cos, self.sin, inverse=True)[:, 0]
         return dk, dv

@@ -55,8 +55,10 @@ def test_fwd_rejects_bad_pointers():
 
 def test_causal_flag_and_scale_checked():
     d = _dims()
-    d.causal = 0
-    assert _fwd(d) == 3
+    d.causal = 2                                # 1 causal, 0 bidirectional, else invalid
+    assert _fwd(d) == 1
+    d.causal = -1
+    assert _fwd(d) == 1
     d = _dims(scale=-1.0)
     assert _fwd(d) == 1
 

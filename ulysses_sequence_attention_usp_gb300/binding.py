@@ -107,15 +107,17 @@ def _check(st, where):
         raise UspError(st, where)
 
 
-def make_dims(S, P, Hq, Hkv, D, cu_seqlens=None, cu_seqlens_host=None, scale=0.0):
+def make_dims(S, P, Hq, Hkv, D, cu_seqlens=None, cu_seqlens_host=None, scale=0.0,
+              causal=True):
     """Build a usp_dims.  ``cu_seqlens`` is a device int32 tensor (or None for
-    one document); ``cu_seqlens_host`` an optional numpy int32 copy.  The
-    returned struct keeps references to both."""
+    one document); ``cu_seqlens_host`` an optional numpy int32 copy;
+    ``causal=False`` selects bidirectional attention within each document.
+    The returned struct keeps references to both arrays."""
     n_docs = 0
     if cu_seqlens is not None:
         n_docs = int(cu_seqlens.numel()) - 1
     d = usp_dims(int(S), int(P), int(Hq), int(Hkv), int(D), _ptr(cu_seqlens),
-                 _ptr(cu_seqlens_host), n_docs, 1, float(scale))
+                 _ptr(cu_seqlens_host), n_docs, 1 if causal else 0, float(scale))
     d._keep = (cu_seqlens, cu_seqlens_host)
     return d
 

@@ -92,6 +92,7 @@ struct Params {
   bf16* dv;
   int64_t S, S_pad, S_ws;
   int hq, hkv, G, n_tiles;
+  int causal;            // 0: every key of a row's document is visible
   float scale, scale_log2;
   unsigned* status;
 };
@@ -464,14 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t u0 = (int64_t)blockIdx.x * BT;
   const int g = blockIdx.y / p.hkv;
   const int jk = blockIdx.y % p.hkv;
-  // query rows that see these keys: [u0, end of the last valid key's document)
+  // query rows that see these keys: from u0 (causal) or the first key's
+  // document start, to the end of the last valid key's document
   int n_q = 0;
   int64_t tq0 = 0;
   {
     const int64_t last = min(u0 + BT, p.S) - 1;
     if (last >= u0) {
       const int64_t e = doc_end_of(p, last);
-      tq0 = (u0 / BT) * BT;
+      tq0 = ((p.causal ? u0 : doc_start_of(p, u0)) / BT) * BT;
       n_q = (int)((e - tq0 + BT - 1) / BT);
     }
   }
@@ -512,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - kEw0) >> 2;       // columns [64*half, 64*half + 64)
     const int r = quarter * 32 + lane;
     const int64_t u = u0 + r;
-    const int64_t de = doc_end_of(p, u);         // queries [u, de) see key u
+    const int64_t de = doc_end_of(p, u);         // queries [qs, de) see key u
+    const int64_t qs = p.causal ? u : doc_start_of(p, u);
     const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
     const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
     // per-query LSE*log2(e) (next to the Q tile) and delta (next to the dO
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = tc::mbar_wait_warp(&bars->sd_full, it & 1, abort);
       if (!ok) break;
       tc::fence_after_sync();
-      const int lo = (int)max((int64_t)0, min((int64_t)BT, u - t0));
+      const int lo = (int)max((int64_t)0, min((int64_t)BT, qs - t0));
       const int hi = de < 0 ? -1 : (int)min((int64_t)BT - 1, de - 1 - t0);
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
       uint32_t pk[32];
@@ -612,7 +615,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t ds0 = doc_start_of(p, t0);
     if (ds0 >= 0) {
       kv_start = (ds0 / BT) * BT;
-      n_kv = (int)((min(t0 + BT, p.S) - kv_start + BT - 1) / BT);
+      const int64_t last = min(t0 + BT, p.S) - 1;
+      const int64_t kv_end = p.causal ? last + 1 : doc_end_of(p, last);
+      n_kv = (int)((kv_end - kv_start + BT - 1) / BT);
     }
   }
 
@@ -646,6 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const int64_t t = t0 + r;
     const int64_t ds = doc_start_of(p, t);
+    // last key row t sees: itself (causal) or its document's last row
+    const int64_t ke = ds < 0 ? -1 : (p.causal ? t : doc_end_of(p, t) - 1);
     float lse2 = INFINITY, dl = 0.f;
     if (ds >= 0) {
       const int64_t li = ((int64_t)g * p.hq + jq) * p.S_ws + t;
@@ -680,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
       const int64_t u0 = kv_start + (int64_t)it * BT;
       const int lo = (int)max((int64_t)0, min((int64_t)BT, ds - u0));
-      const int hi = ds < 0 ? -1 : (int)min((int64_t)BT - 1, t - u0);
+      const int hi = ds < 0 ? -1 : (int)max((int64_t)-1, min((int64_t)BT - 1, ke - u0));
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
       const uint32_t tRb = tR;
       ok = mask ? dq_half<true>(tS, tP, tRb, half, lo, hi, lse2, dl, p.scale_log2, bars, it, abort)
@@ -842,6 +849,7 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
   prm.hq = g.hq;
   prm.hkv = g.hkv;
   prm.G = g.G;
+  prm.causal = g.causal;
   prm.n_tiles = (int)((g.S_pad + BT - 1) / BT);
   prm.scale = g.scale;
   prm.scale_log2 = g.scale * kLog2e;

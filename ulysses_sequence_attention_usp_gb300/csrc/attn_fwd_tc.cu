@@ -62,6 +62,7 @@ struct Params {
   float* lse;
   int64_t S, S_pad;
   int hq, hkv, G, n_qtiles, slots_per_kv;
+  int causal;             // 0: every key of the row's document is visible
   float scale_log2;
   unsigned* status;
 };
@@ -82,6 +83,13 @@ __device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
   const int d = __ldg(p.doc + t);
   if (d < 0) return -1;
   return p.cu ? (int64_t)__ldg(p.cu + d) : 0;
+}
+// One past the last row of t's document (-1 for a pad row).
+__device__ __forceinline__ int64_t doc_end_of(const Params& p, int64_t t) {
+  if (t >= p.S) return -1;
+  const int d = __ldg(p.doc + t);
+  if (d < 0) return -1;
+  return p.cu ? (int64_t)__ldg(p.cu + d + 1) : p.S;
 }
 
 // One softmax step on this thread's S row: the 128 fp32 columns are read
@@ -150,14 +158,15 @@ __global__ void __launch_bounds__(384, 1)
   const int64_t t0 = (int64_t)qt * BM;
 
   // kv range needed by the tile: from the first row's document start up to
-  // its last valid row
+  // its last valid row (causal) or to the end of that row's document
   int n_kv = 0;
   int64_t kv_start = 0;
   {
     const int64_t ds0 = doc_start_of(p, t0);
     if (ds0 >= 0) {
       kv_start = (ds0 / BN) * BN;
-      const int64_t kv_end = min(t0 + BM, p.S);
+      const int64_t last = min(t0 + BM, p.S) - 1;
+      const int64_t kv_end = p.causal ? last + 1 : doc_end_of(p, last);
       n_kv = (int)((kv_end - kv_start + BN - 1) / BN);
     }
   }
@@ -288,6 +297,8 @@ __global__ void __launch_bounds__(384, 1)
     const int j = j0 + h;
     if (h < NH) {
       const int64_t ds = doc_start_of(p, t);    // -1: row sees nothing
+      // last visible key: the row itself (causal) or its document's last row
+      const int64_t ke = ds < 0 ? -1 : (p.causal ? t : doc_end_of(p, t) - 1);
       const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, C::S_COL(h));
       const uint32_t tO = tc::tmem_addr(tmem, quarter * 32, C::O_COL(h));
       float m = -INFINITY, l = 0.f;
@@ -297,11 +308,11 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         tc::fence_after_sync();
         const int64_t u0 = kv_start + (int64_t)jt * BN;
-        const bool row_mask = ds < 0 || u0 < ds || u0 + BN - 1 > t;
+        const bool row_mask = ds < 0 || u0 < ds || u0 + BN - 1 > ke;
         const bool mask = __any_sync(0xffffffffu, row_mask);
-        // keys u0+c visible to row t iff ds <= u0+c <= t  (c in [lo, hi])
+        // keys u0+c visible to row t iff ds <= u0+c <= ke  (c in [lo, hi])
         const int lo = (int)max((int64_t)0, min((int64_t)BN, ds - u0));
-        const int hi = ds < 0 ? -1 : (int)min((int64_t)BN - 1, t - u0);
+        const int hi = ds < 0 ? -1 : (int)max((int64_t)-1, min((int64_t)BN - 1, ke - u0));
         // the mask is warp-uniform, so fully visible tiles take the path
         // without per-column tests
         bool rescale = false;
@@ -446,6 +457,7 @@ cudaError_t usp_launch_attn_fwd(const usp::Geometry& g, const void* q, const voi
   prm.G = g.G;
   prm.n_qtiles = (int)((g.S_pad + BM - 1) / BM);
   prm.slots_per_kv = g.G / nh;
+  prm.causal = g.causal;
   prm.scale_log2 = g.scale * kLog2e;
   prm.status = g.status;
   if (g.D == 128)

@@ -44,7 +44,7 @@ usp_status geometry(const usp_dims* d, usp::Geometry* g) {
   if (d->Hq < 1 || d->Hkv < 1) return USP_ERR_INVALID_ARG;
   if (d->Hq % d->P || d->Hkv % d->P || d->Hq % d->Hkv) return USP_ERR_HEADS_NOT_DIVISIBLE;
   if (d->D != 64 && d->D != 128) return USP_ERR_UNSUPPORTED;
-  if (d->causal != 1) return USP_ERR_UNSUPPORTED;
+  if (d->causal != 0 && d->causal != 1) return USP_ERR_INVALID_ARG;
   if (d->cu_seqlens != nullptr && d->n_docs < 1) return USP_ERR_INVALID_ARG;
   if (!(d->scale >= 0.f) || isinf(d->scale)) return USP_ERR_INVALID_ARG;
   const int64_t S_pad = (d->S + d->P - 1) / d->P * d->P;
@@ -58,6 +58,7 @@ usp_status geometry(const usp_dims* d, usp::Geometry* g) {
   }
   g->S = d->S;
   g->P = d->P;
+  g->causal = d->causal;
   g->S_pad = S_pad;
   g->S_loc = S_pad / d->P;
   g->Hq = d->Hq;

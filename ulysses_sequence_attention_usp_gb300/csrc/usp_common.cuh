@@ -22,6 +22,7 @@ __device__ __forceinline__ void set_status(unsigned* word, unsigned bits) {
 struct Geometry {
   int64_t S, S_pad, S_loc;
   int P, Hq, Hkv, D, hq, hkv, G;
+  int causal;            // 1: keys u <= t of the document; 0: the whole document
   float scale;
   unsigned* status;   // device address of the status word of the current device
 };

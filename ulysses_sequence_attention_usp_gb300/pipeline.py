@@ -23,14 +23,16 @@ from . import binding as B
 
 class UlyssesAttention:
     def __init__(self, S, P, Hq, Hkv, D, cu_seqlens=None, rope_base=1.0e4, yarn_factor=1.0,
-                 yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None):
+                 yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None,
+                 causal=True):
         self.S, self.P, self.Hq, self.Hkv, self.D = int(S), int(P), int(Hq), int(Hkv), int(D)
         self.S_pad = -(-self.S // self.P) * self.P
         self.device = torch.device(device)
         dev = self.device
         self.cu_host = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, np.int32)
         self.cu_dev = None if self.cu_host is None else torch.from_numpy(self.cu_host).to(dev)
-        self.dims = B.make_dims(S, P, Hq, Hkv, D, self.cu_dev, self.cu_host, scale)
+        self.causal = bool(causal)
+        self.dims = B.make_dims(S, P, Hq, Hkv, D, self.cu_dev, self.cu_host, scale, causal)
         self.rope_len = int(rope_len) if rope_len else self.S_pad
         if rope_table is None:
             rope_table = B.usp_rope_table(self.rope_len, D, rope_base, yarn_factor, yarn_orig_ctx)
