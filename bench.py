@@ -102,11 +102,11 @@ def aggregate_throughput(world, tokens_per_rank, steps, seconds):
     return world * tokens_per_rank * steps / seconds
 
 
-def causal_pairs(S, cu):
-    if cu is None:
-        return S * (S + 1) // 2
-    lens = np.diff(np.asarray(cu, np.int64))
-    return int((lens * (lens + 1) // 2).sum())
+def attended_pairs(S, cu, causal=True):
+    """(query, key) pairs attended: per document L(L+1)/2 causal, L^2
+    bidirectional."""
+    lens = np.array([S], np.int64) if cu is None else np.diff(np.asarray(cu, np.int64))
+    return int((lens * (lens + 1) // 2).sum()) if causal else int((lens * lens).sum())
 
 
 class ClockSampler:
@@ -177,7 +177,7 @@ def gpu_bus_id(torch):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample(wl, inp, target_s, fixed_rows=None):
+def oracle_sample(wl, inp, target_s, fixed_rows=None, causal=True):
     """Time the oracle's forward+backward of query head 0 (and its KV head)
     on the first S' rows, S' grown until one run takes about target_s
     seconds (or S' = fixed_rows).  Returns (seconds, S', scale factor to the
@@ -198,13 +198,13 @@ def oracle_sample(wl, inp, target_s, fixed_rows=None):
         if inp.cu is not None:
             cu = np.concatenate([inp.cu[inp.cu < Sp], [Sp]]).astype(np.int64)
         t0 = time.perf_counter()
-        O.full_sequence(q, k, v, do, cu, cos, sin, scale)
+        O.full_sequence(q, k, v, do, cu, cos, sin, scale, causal)
         dt = time.perf_counter() - t0
         if fixed_rows or dt >= target_s / 3 or Sp >= wl.S:
             break
         Sp = int(Sp * min(4.0, max(1.3, math.sqrt(target_s / max(dt, 1e-3)))))
-    pairs_s = causal_pairs(Sp, cu)
-    pairs_f = causal_pairs(wl.S, inp.cu)
+    pairs_s = attended_pairs(Sp, cu, causal)
+    pairs_f = attended_pairs(wl.S, inp.cu, causal)
     factor = (pairs_f * wl.Hq) / pairs_s
     return dt, Sp, factor
 
@@ -222,22 +222,23 @@ def run_reference(args, wl, inp):
     if rank != 0:
         return
     times = []
-    _, Sp, factor = oracle_sample(wl, inp, args.ref_seconds)
+    causal = not args.bidirectional
+    _, Sp, factor = oracle_sample(wl, inp, args.ref_seconds, causal=causal)
     for i in range(args.warmup + args.steps):
-        dt, Sp, factor = oracle_sample(wl, inp, args.ref_seconds, fixed_rows=Sp)
+        dt, Sp, factor = oracle_sample(wl, inp, args.ref_seconds, fixed_rows=Sp, causal=causal)
         if i >= args.warmup:
             times.append(dt * factor)
     full_s = statistics.median(times)
     value = wl.S / full_s
     sample = (f"oracle fwd+bwd of q head 0 / kv head 0 on the first {Sp} rows, "
-              f"scaled by causal pairs x heads ({factor:.4g}x) to the full workload")
+              f"scaled by attended pairs x heads ({factor:.4g}x) to the full workload")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": full_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "S": wl.S, "P": wl.P, "Hq": wl.Hq, "Hkv": wl.Hkv,
-                   "D": wl.D},
+                   "D": wl.D, "attention": "causal" if causal else "bidirectional"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -267,9 +268,11 @@ def run_usp(args, wl, inp):
     def to_dev(bits):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
 
+    causal = not args.bidirectional
     ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
                           rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
-                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev)
+                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
+                          causal=causal)
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     st = torch.cuda.current_stream(dev)
     d = ua.dims
@@ -345,7 +348,7 @@ def run_usp(args, wl, inp):
     ua2 = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
                            rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
                            yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
-                           rope_table=ua.rope_host)
+                           rope_table=ua.rope_host, causal=causal)
     pipes = [(ua, (q, k, v, do)), (ua2, tuple(torch.empty_like(t) for t in (q, k, v, do)))]
     h_out = [[torch.empty(t.shape, dtype=torch.int16).pin_memory()
               for t in (ua.o, ua.dq, ua.dk, ua.dv)] for _ in range(2)]
@@ -396,7 +399,7 @@ def run_usp(args, wl, inp):
 
     if rank == 0:
         peaks, src = load_peaks()
-        pairs = causal_pairs(wl.S, inp.cu)
+        pairs = attended_pairs(wl.S, inp.cu, causal)
         f_fwd = 4.0 * wl.D * wl.Hq * pairs
         f_bwd = 10.0 * wl.D * wl.Hq * pairs
         step_s = elapsed / args.steps
@@ -420,6 +423,7 @@ def run_usp(args, wl, inp):
             "config": {"workload": wl.name, "S": wl.S, "P": wl.P, "Hq": wl.Hq, "Hkv": wl.Hkv,
                        "D": wl.D, "rope": ("yarn x%g to %d" % (wl.yarn_factor, wl.rope_len)
                                            if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
+                       "attention": "causal" if causal else "bidirectional",
                        "parallelism": f"replicas x{world} (P={wl.P} virtual shards per GPU)",
                        "l2": "inputs larger than L2 (Q alone %.2f GB); no flush" % (bq / 1e9)},
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
@@ -432,7 +436,7 @@ def run_usp(args, wl, inp):
                           "fwd_frac": f_fwd / t_fwd / 1e12 / peak_t,
                           "fwd_bwd_tflops": (f_fwd + f_bwd) / (t_fwd + t_bwd) / 1e12,
                           "fwd_ms": t_fwd * 1e3, "bwd_ms": t_bwd * 1e3,
-                          "causal_pairs": pairs},
+                          "attended_pairs": pairs},
             "repack": {"gbps": rep_gbs, "frac": rep_gbs / peaks["hbm_gbs"],
                        "peak_gbps": peaks["hbm_gbs"], "peak_source": src,
                        "bytes_per_step": sum(rep_bytes.values())},
@@ -445,12 +449,12 @@ def run_usp(args, wl, inp):
             "clocks": clk,
         }
         if world == 1 and not args.no_cpu_baseline:
-            dt, Sp, factor = oracle_sample(wl, inp, args.cpu_seconds)
+            dt, Sp, factor = oracle_sample(wl, inp, args.cpu_seconds, causal=causal)
             line["cpu_baseline"] = {
                 "value": wl.S / (dt * factor), "unit": "tokens/s", "cores": cpu_cores(),
                 "kind": "oracle",
                 "sample": (f"oracle fwd+bwd of q head 0 / kv head 0 on the first {Sp} rows "
-                           f"({dt:.1f} s), scaled by causal pairs x heads ({factor:.4g}x)")}
+                           f"({dt:.1f} s), scaled by attended pairs x heads ({factor:.4g}x)")}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
@@ -467,6 +471,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bidirectional", action="store_true",
+                    help="attention over the whole document (causal = 0)")
     args = ap.parse_args()
     from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, make_inputs
     wl = WORKLOADS[args.workload]
