@@ -85,16 +85,80 @@ def shard_pad(x: np.ndarray, P: int) -> np.ndarray:
     return out
 
 
-def positions_docs(S: int, P: int, cu=None):
+# ---------------------------------------------------------------------------
+# Zigzag partition (Megatron-LM PR #7 "GLM-5.2 131k context parallelism",
+# closing comment: upstream replaced the contiguous partition by a zigzag
+# one).  Reading: the padded sequence is cut into 2P equal chunks and rank r
+# holds chunks r and 2P-1-r, in that order, so every rank gets the same
+# share of causal work.  Rows stay global everywhere else: positions,
+# documents and the head layout after the all-to-all are in global order.
+# ---------------------------------------------------------------------------
+
+
+def zigzag_padded_len(S: int, P: int) -> int:
+    """S rounded up to a multiple of 2P (2P equal chunks)."""
+    return -(-S // (2 * P)) * (2 * P)
+
+
+def zigzag_order(S_pad: int, P: int) -> np.ndarray:
+    """order[i] = global row held at row i of the sharded buffer, i = r*2C + s
+    for rank r and local row s (C = S_pad / 2P)."""
+    C = S_pad // (2 * P)
+    order = np.zeros(S_pad, dtype=np.int64)
+    for r in range(P):
+        for s in range(2 * C):
+            chunk = r if s < C else 2 * P - 1 - r
+            order[r * 2 * C + s] = chunk * C + (s % C)
+    return order
+
+
+def shard_pad_zigzag(x: np.ndarray, P: int) -> np.ndarray:
+    """[S][H][D] -> [S_pad][H][D] in zigzag shard order; rows of the padding
+    (global rows >= S) are zero."""
+    S = x.shape[0]
+    S_pad = zigzag_padded_len(S, P)
+    out = np.zeros((S_pad,) + x.shape[1:], dtype=x.dtype)
+    for i, t in enumerate(zigzag_order(S_pad, P)):
+        if t < S:
+            out[i] = x[t]
+    return out
+
+
+def seq_to_head_zigzag(x_seq: np.ndarray, P: int) -> np.ndarray:
+    """All-to-all from zigzag shards to head groups in global row order:
+    X_head[g][order[i]][j] = X_seq[i][g*H/P + j]."""
+    S_pad, H, D = x_seq.shape
+    hp = H // P
+    out = np.zeros((P, S_pad, hp, D), dtype=x_seq.dtype)
+    order = zigzag_order(S_pad, P)
+    for i in range(S_pad):
+        for g in range(P):
+            out[g, order[i]] = x_seq[i, g * hp:(g + 1) * hp]
+    return out
+
+
+def head_to_seq_zigzag(x_head: np.ndarray) -> np.ndarray:
+    """Inverse of :func:`seq_to_head_zigzag`."""
+    P, S_pad, hp, D = x_head.shape
+    out = np.zeros((S_pad, P * hp, D), dtype=x_head.dtype)
+    order = zigzag_order(S_pad, P)
+    for i in range(S_pad):
+        for g in range(P):
+            out[i, g * hp:(g + 1) * hp] = x_head[g, order[i]]
+    return out
+
+
+def positions_docs(S: int, P: int, cu=None, S_pad=None):
     """Absolute positions and document ids of the S_pad padded rows.
 
     Row t < S belongs to document d with cu[d] <= t < cu[d+1] and has position
     t - cu[d] (positions restart at documents, never at shard boundaries).
     Pad rows t >= S get doc -1 and keep counting inside the last document, so
     the RoPE table has to cover S_pad positions.  ``cu=None`` means one
-    document [0, S).
+    document [0, S).  ``S_pad`` overrides the padded length (the zigzag
+    partition pads to a multiple of 2P).
     """
-    S_pad = padded_len(S, P)
+    S_pad = padded_len(S, P) if S_pad is None else S_pad
     cu = np.array([0, S], dtype=np.int64) if cu is None else np.asarray(cu, np.int64)
     assert cu[0] == 0 and cu[-1] == S and np.all(np.diff(cu) >= 0)
     pos = np.zeros(S_pad, dtype=np.int64)
@@ -376,15 +440,23 @@ def full_sequence(q, k, v, do, cu, cos, sin, scale, causal=True):
     return dict(o=o, lse=lse, loss=float((o * do).sum()), dq=dq, dk=dk, dv=dv)
 
 
-def ulysses(q, k, v, do, cu, cos, sin, scale, P, causal=True):
+def ulysses(q, k, v, do, cu, cos, sin, scale, P, causal=True, zigzag=False):
     """The Ulysses path: pad and shard, all-to-all to head groups, RoPE at
-    absolute positions, attention per head group, all-to-all back."""
+    absolute positions, attention per head group, all-to-all back.  With
+    ``zigzag`` the shards are the zigzag partition (the head layout is the
+    same global-order layout either way)."""
     S, Hq, D = q.shape
     Hkv = k.shape[1]
     check_heads(P, Hq, Hkv)
-    pos, doc = positions_docs(S, P, cu)
-    heads = {n: seq_to_head(shard_pad(x, P), P)
-             for n, x in (("q", q), ("k", k), ("v", v), ("do", do))}
+    if zigzag:
+        pos, doc = positions_docs(S, P, cu, S_pad=zigzag_padded_len(S, P))
+        to_head = lambda x: seq_to_head_zigzag(shard_pad_zigzag(x, P), P)  # noqa: E731
+        to_seq = lambda x: head_to_seq_zigzag(x)[np.argsort(zigzag_order(x.shape[1], P))]  # noqa: E731,E501
+    else:
+        pos, doc = positions_docs(S, P, cu)
+        to_head = lambda x: seq_to_head(shard_pad(x, P), P)  # noqa: E731
+        to_seq = head_to_seq
+    heads = {n: to_head(x) for n, x in (("q", q), ("k", k), ("v", v), ("do", do))}
     S_pad = pos.shape[0]
     hq, hkv = Hq // P, Hkv // P
     o_h = np.zeros((P, S_pad, hq, D))
@@ -401,8 +473,8 @@ def ulysses(q, k, v, do, cu, cos, sin, scale, P, causal=True):
         dq_h[g] = rope_rotate(a, pos, cos, sin, inverse=True)
         dk_h[g] = rope_rotate(b, pos, cos, sin, inverse=True)
         dv_h[g] = c
-    o = head_to_seq(o_h)[:S]
+    # back to sequence layout, then to global row order for the comparison
+    o = to_seq(o_h)[:S]
     lse = lse_h.reshape(Hq, S_pad)[:, :S]
     return dict(o=o, lse=lse, loss=float((o * do).sum()),
-                dq=head_to_seq(dq_h)[:S], dk=head_to_seq(dk_h)[:S],
-                dv=head_to_seq(dv_h)[:S])
+                dq=to_seq(dq_h)[:S], dk=to_seq(dk_h)[:S], dv=to_seq(dv_h)[:S])
