@@ -83,6 +83,17 @@ typedef struct {
                                        Ulysses); anything else is
                                        USP_ERR_INVALID_ARG */
   float scale;                      /* softmax scale; 0 => 1/sqrt(D) */
+  int32_t zigzag;                   /* shard layout of the sequence-sharded
+                                       buffers: 0 contiguous (rank r holds
+                                       rows [r*S_pad/P, (r+1)*S_pad/P)); 1
+                                       zigzag (Megatron-LM #7, closing
+                                       comment): S_pad is a multiple of 2P,
+                                       the sequence is cut into 2P equal
+                                       chunks and rank r holds chunks r and
+                                       2P-1-r, in that order.  Anything else
+                                       is USP_ERR_INVALID_ARG.  Head-layout
+                                       buffers, pos and doc are in global row
+                                       order either way. */
 } usp_dims;
 
 /*
@@ -93,8 +104,11 @@ typedef struct {
  * alignment; Megatron-LM #7, Purpose: positions from the GLOBAL cu_seqlens.)
  *
  *   x     [S][H][D] bf16 (input, unpadded)
- *   x_seq [S_pad][H][D] bf16 (output): rows < S copied, rows >= S zero.
- *         x_seq == x is allowed (in place; the buffer must hold S_pad rows).
+ *   x_seq [S_pad][H][D] bf16 (output): rows < S copied, rows >= S zero;
+ *         with zigzag, row r*(S_pad/P) + s holds global row
+ *         (s < C ? r : 2P-1-r)*C + s % C, C = S_pad/(2P).
+ *         x_seq == x is allowed for the contiguous layout (in place; the
+ *         buffer must hold S_pad rows), not for zigzag.
  *   pos   [S_pad] int32 or NULL: t - cu[doc(t)]; pad rows keep counting in
  *         the last document.
  *   doc   [S_pad] int32 or NULL: document index of row t, -1 for pad rows.
@@ -108,7 +122,8 @@ usp_status usp_pad_shard(const usp_dims* dims, const void* x, int32_t H,
  * Modifications: separate Q/K/V all-to-alls before local attention), fused
  * with RoPE at absolute positions.
  *
- *   x_seq  [S_pad][H][D] bf16 -> x_head [P][S_pad][H/P][D] bf16
+ *   x_seq  [S_pad][H][D] bf16 (shard layout of dims->zigzag) -> x_head
+ *          [P][S_pad][H/P][D] bf16 in global row order
  *   rope_mode 0: plain permutation (V, dO); pos/rope_cs may be NULL.
  *   rope_mode 1: rotate every (d, d+D/2) pair of row t by the table entry
  *                at pos[t]; -1 rotates by the negated angle.

@@ -61,6 +61,16 @@ def test_causal_flag_and_scale_checked():
     assert _fwd(d) == 1
     d = _dims(scale=-1.0)
     assert _fwd(d) == 1
+    d = _dims()
+    d.zigzag = 2                                # 0 contiguous, 1 zigzag, else invalid
+    assert _fwd(d) == 1
+
+
+def test_zigzag_pad_shard_cannot_run_in_place():
+    d = _dims()
+    d.zigzag = 1
+    st = B.raw_call("usp_pad_shard", ctypes.byref(d), FAKE, 2, FAKE, None, None, None)
+    assert st == 1
 
 
 def test_bwd_workspace_size_and_checks():

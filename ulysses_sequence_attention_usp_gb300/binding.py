@@ -40,7 +40,7 @@ class usp_dims(ctypes.Structure):
                 ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32),
                 ("cu_seqlens", ctypes.c_void_p), ("cu_seqlens_host", ctypes.c_void_p),
                 ("n_docs", ctypes.c_int32), ("causal", ctypes.c_int32),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("zigzag", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -108,16 +108,18 @@ def _check(st, where):
 
 
 def make_dims(S, P, Hq, Hkv, D, cu_seqlens=None, cu_seqlens_host=None, scale=0.0,
-              causal=True):
+              causal=True, zigzag=False):
     """Build a usp_dims.  ``cu_seqlens`` is a device int32 tensor (or None for
     one document); ``cu_seqlens_host`` an optional numpy int32 copy;
-    ``causal=False`` selects bidirectional attention within each document.
+    ``causal=False`` selects bidirectional attention within each document;
+    ``zigzag=True`` the zigzag shard layout of the sequence-sharded buffers.
     The returned struct keeps references to both arrays."""
     n_docs = 0
     if cu_seqlens is not None:
         n_docs = int(cu_seqlens.numel()) - 1
     d = usp_dims(int(S), int(P), int(Hq), int(Hkv), int(D), _ptr(cu_seqlens),
-                 _ptr(cu_seqlens_host), n_docs, 1 if causal else 0, float(scale))
+                 _ptr(cu_seqlens_host), n_docs, 1 if causal else 0, float(scale),
+                 1 if zigzag else 0)
     d._keep = (cu_seqlens, cu_seqlens_host)
     return d
 

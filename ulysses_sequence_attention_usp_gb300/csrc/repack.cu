@@ -13,6 +13,8 @@
 //
 // Both kernels are HBM-bound: 16-byte loads and stores, streaming cache
 // hints, one warp per token row and several heads in flight per thread.
+// The sequence-sharded side may use the zigzag shard layout; it only
+// changes which buffer row holds global row t.
 #include "usp_common.cuh"
 
 namespace {
@@ -24,6 +26,21 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 }
 __device__ __forceinline__ void st_stream(void* p, uint4 v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// Zigzag shard layout (Megatron-LM PR #7, closing comment): 2P chunks of C
+// rows; rank r holds chunks r and 2P-1-r, so global row t sits at row
+// zz_row(t) of the sharded buffer and buffer row i holds global row
+// zz_global(i).  C = 0 means the contiguous layout (row t at row t).
+__device__ __forceinline__ int64_t zz_row(int64_t t, int64_t C, int P) {
+  if (C == 0) return t;
+  const int64_t c = t / C, s = t - c * C;
+  return c < P ? c * 2 * C + s : (2 * P - 1 - c) * 2 * C + C + s;
+}
+__device__ __forceinline__ int64_t zz_global(int64_t i, int64_t C, int P) {
+  if (C == 0) return i;
+  const int64_t r = i / (2 * C), s = i - r * 2 * C;
+  return s < C ? r * C + s : (2 * P - 1 - r) * C + (s - C);
 }
 
 // ---------------------------------------------------------------- pad/shard
@@ -40,15 +57,24 @@ __device__ __forceinline__ int doc_of(const int32_t* cu, int n_docs, int64_t t) 
 __global__ void __launch_bounds__(256) pad_shard_kernel(
     const uint4* __restrict__ x, uint4* __restrict__ y, int64_t n_valid_vec,
     int64_t n_total_vec, int inplace, int32_t* __restrict__ pos, int32_t* __restrict__ doc,
-    const int32_t* __restrict__ cu, int n_docs, int64_t S, int64_t S_pad) {
+    const int32_t* __restrict__ cu, int n_docs, int64_t S, int64_t S_pad, int64_t row_vec,
+    int64_t zz_chunk, int P) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int64_t i = i0; i < n_total_vec; i += stride) {
-    if (i < n_valid_vec) {
-      if (!inplace) st_stream(y + i, ld_stream(x + i));
-    } else {
-      st_stream(y + i, zero);
+  if (zz_chunk == 0) {
+    for (int64_t i = i0; i < n_total_vec; i += stride) {
+      if (i < n_valid_vec) {
+        if (!inplace) st_stream(y + i, ld_stream(x + i));
+      } else {
+        st_stream(y + i, zero);
+      }
+    }
+  } else {   // buffer row r holds global row zz_global(r): a row permutation
+    for (int64_t i = i0; i < n_total_vec; i += stride) {
+      const int64_t r = i / row_vec, c = i - r * row_vec;
+      const int64_t t = zz_global(r, zz_chunk, P);
+      st_stream(y + i, t < S ? ld_stream(x + t * row_vec + c) : zero);
     }
   }
   if (pos == nullptr && doc == nullptr) return;
@@ -73,7 +99,7 @@ template <int D, int MODE, bool TO_HEAD>
 __global__ void __launch_bounds__(256) repack_kernel(
     const bf16* __restrict__ src, bf16* __restrict__ dst, const int32_t* __restrict__ pos,
     const float* __restrict__ cs, int64_t rope_len, int64_t S_pad, int H, int hp,
-    unsigned* status) {
+    unsigned* status, int64_t zz_chunk, int P) {
   constexpr int TPH = D / 16;
   constexpr int HPI = 32 / TPH;
   constexpr int kUnroll = 4;
@@ -84,6 +110,7 @@ __global__ void __launch_bounds__(256) repack_kernel(
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
 
   for (int64_t t = warp; t < S_pad; t += nwarps) {
+    const int64_t srow = zz_row(t, zz_chunk, P);   // row of t in the sharded buffer
     float c[8], s[8];
     bool zero_row = false;
     if (MODE != 0) {
@@ -115,7 +142,7 @@ __global__ void __launch_bounds__(256) repack_kernel(
         doff[u] = -1;
         if (h < H) {
           const int g = h / hp, j = h - g * hp;
-          const int64_t seq_off = (t * H + h) * (int64_t)D;
+          const int64_t seq_off = (srow * H + h) * (int64_t)D;
           const int64_t head_off = (((int64_t)g * S_pad + t) * hp + j) * (int64_t)D;
           const bf16* sp = src + (TO_HEAD ? seq_off : head_off);
           doff[u] = TO_HEAD ? head_off : seq_off;
@@ -162,14 +189,17 @@ int repack_grid(int64_t S_pad) {
 template <int D, bool TO_HEAD>
 cudaError_t launch_mode(int mode, const bf16* src, bf16* dst, const int32_t* pos,
                         const float* cs, int64_t rope_len, int64_t S_pad, int H, int hp,
-                        unsigned* status, cudaStream_t st) {
+                        unsigned* status, int64_t zz, int P, cudaStream_t st) {
   const int grid = repack_grid(S_pad);
   if (mode == 0)
-    repack_kernel<D, 0, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp, status);
+    repack_kernel<D, 0, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp,
+                                                       status, zz, P);
   else if (mode > 0)
-    repack_kernel<D, 1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp, status);
+    repack_kernel<D, 1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp,
+                                                       status, zz, P);
   else
-    repack_kernel<D, -1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp, status);
+    repack_kernel<D, -1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H,
+                                                        hp, status, zz, P);
   usp_count_launches(1);
   return cudaGetLastError();
 }
@@ -188,7 +218,7 @@ cudaError_t usp_launch_pad_shard(const usp::Geometry& g, const void* x, int H, v
   if (blocks < 1) blocks = 1;
   pad_shard_kernel<<<(int)blocks, 256, 0, st>>>(
       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_seq), n_valid, n_total,
-      x == x_seq ? 1 : 0, pos, doc, cu, n_docs, g.S, g.S_pad);
+      x == x_seq ? 1 : 0, pos, doc, cu, n_docs, g.S, g.S_pad, row_vec, g.zz_chunk, g.P);
   usp_count_launches(1);
   return cudaGetLastError();
 }
@@ -199,9 +229,14 @@ cudaError_t usp_launch_repack(const usp::Geometry& g, const void* src, int H, co
   const int hp = H / g.P;
   const bf16* s = reinterpret_cast<const bf16*>(src);
   bf16* d = reinterpret_cast<bf16*>(dst);
+  const int64_t zz = g.zz_chunk;
   if (g.D == 128)
-    return to_head ? launch_mode<128, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st)
-                   : launch_mode<128, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st);
-  return to_head ? launch_mode<64, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st)
-                 : launch_mode<64, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp, g.status, st);
+    return to_head ? launch_mode<128, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H,
+                                            hp, g.status, zz, g.P, st)
+                   : launch_mode<128, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H,
+                                             hp, g.status, zz, g.P, st);
+  return to_head ? launch_mode<64, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp,
+                                         g.status, zz, g.P, st)
+                 : launch_mode<64, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H,
+                                          hp, g.status, zz, g.P, st);
 }

@@ -45,9 +45,11 @@ usp_status geometry(const usp_dims* d, usp::Geometry* g) {
   if (d->Hq % d->P || d->Hkv % d->P || d->Hq % d->Hkv) return USP_ERR_HEADS_NOT_DIVISIBLE;
   if (d->D != 64 && d->D != 128) return USP_ERR_UNSUPPORTED;
   if (d->causal != 0 && d->causal != 1) return USP_ERR_INVALID_ARG;
+  if (d->zigzag != 0 && d->zigzag != 1) return USP_ERR_INVALID_ARG;
   if (d->cu_seqlens != nullptr && d->n_docs < 1) return USP_ERR_INVALID_ARG;
   if (!(d->scale >= 0.f) || isinf(d->scale)) return USP_ERR_INVALID_ARG;
-  const int64_t S_pad = (d->S + d->P - 1) / d->P * d->P;
+  const int64_t unit = d->zigzag ? 2 * (int64_t)d->P : (int64_t)d->P;
+  const int64_t S_pad = (d->S + unit - 1) / unit * unit;
   if (S_pad > (int64_t)INT32_MAX) return USP_ERR_UNSUPPORTED;   // positions are int32
   if (d->cu_seqlens_host != nullptr) {
     const int32_t* cu = d->cu_seqlens_host;
@@ -61,6 +63,7 @@ usp_status geometry(const usp_dims* d, usp::Geometry* g) {
   g->causal = d->causal;
   g->S_pad = S_pad;
   g->S_loc = S_pad / d->P;
+  g->zz_chunk = d->zigzag ? S_pad / (2 * (int64_t)d->P) : 0;
   g->Hq = d->Hq;
   g->Hkv = d->Hkv;
   g->D = d->D;
@@ -127,6 +130,7 @@ usp_status usp_pad_shard(const usp_dims* dims, const void* x, int32_t H, void* x
   if (H == 0 && (x != nullptr || x_seq != nullptr)) return USP_ERR_INVALID_ARG;
   if ((x && !aligned16(x)) || (x_seq && !aligned16(x_seq))) return USP_ERR_INVALID_ARG;
   if (((uintptr_t)pos & 3u) || ((uintptr_t)doc & 3u)) return USP_ERR_INVALID_ARG;
+  if (g.zz_chunk > 0 && x != nullptr && x == x_seq) return USP_ERR_INVALID_ARG;
   if (g.S_pad == 0) return USP_OK;
   return cuda_status(usp_launch_pad_shard(g, x, H, H > 0 ? x_seq : nullptr, pos, doc,
                                           dims->cu_seqlens, dims->n_docs,

@@ -24,15 +24,18 @@ from . import binding as B
 class UlyssesAttention:
     def __init__(self, S, P, Hq, Hkv, D, cu_seqlens=None, rope_base=1.0e4, yarn_factor=1.0,
                  yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None,
-                 causal=True):
+                 causal=True, zigzag=False):
         self.S, self.P, self.Hq, self.Hkv, self.D = int(S), int(P), int(Hq), int(Hkv), int(D)
-        self.S_pad = -(-self.S // self.P) * self.P
+        unit = 2 * self.P if zigzag else self.P      # zigzag: 2P equal chunks
+        self.S_pad = -(-self.S // unit) * unit
+        self.zigzag = bool(zigzag)
         self.device = torch.device(device)
         dev = self.device
         self.cu_host = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, np.int32)
         self.cu_dev = None if self.cu_host is None else torch.from_numpy(self.cu_host).to(dev)
         self.causal = bool(causal)
-        self.dims = B.make_dims(S, P, Hq, Hkv, D, self.cu_dev, self.cu_host, scale, causal)
+        self.dims = B.make_dims(S, P, Hq, Hkv, D, self.cu_dev, self.cu_host, scale, causal,
+                                zigzag)
         self.rope_len = int(rope_len) if rope_len else self.S_pad
         if rope_table is None:
             rope_table = B.usp_rope_table(self.rope_len, D, rope_base, yarn_factor, yarn_orig_ctx)
@@ -57,7 +60,8 @@ class UlyssesAttention:
     # -- steps -------------------------------------------------------------
     def forward(self, q, k, v, stream=None):
         """q [S][Hq][D], k/v [S][Hkv][D] bf16 device tensors (pre-RoPE).
-        Returns O [S_pad][Hq][D] (rows >= S are 0) in sequence layout."""
+        Returns O [S_pad][Hq][D] in the sequence-sharded layout (global row
+        order, or zigzag shard order when zigzag=True); padding rows are 0."""
         d, st = self.dims, stream
         B.usp_pad_shard(d, q, self.Hq, self.q_seq, self.pos, self.doc, st)
         B.usp_pad_shard(d, k, self.Hkv, self.k_seq, None, None, st)
@@ -73,7 +77,8 @@ class UlyssesAttention:
 
     def backward(self, do, stream=None):
         """do [S][Hq][D] bf16 (dL/dO).  Returns dQ, dK, dV [S_pad][H][D]: the
-        gradients of the pre-RoPE sequence-sharded inputs."""
+        gradients of the pre-RoPE sequence-sharded inputs, in the same shard
+        layout as O."""
         d, st = self.dims, stream
         B.usp_pad_shard(d, do, self.Hq, self.do_seq, None, None, st)
         B.usp_seq_to_head_rope(d, self.do_seq, self.Hq, None, None, 0, 0, self.do_h, st)
