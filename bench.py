@@ -272,7 +272,7 @@ def run_usp(args, wl, inp):
     ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
                           rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
                           yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
-                          causal=causal)
+                          causal=causal, zigzag=args.zigzag)
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     st = torch.cuda.current_stream(dev)
     d = ua.dims
@@ -348,7 +348,7 @@ def run_usp(args, wl, inp):
     ua2 = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
                            rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
                            yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
-                           rope_table=ua.rope_host, causal=causal)
+                           rope_table=ua.rope_host, causal=causal, zigzag=args.zigzag)
     pipes = [(ua, (q, k, v, do)), (ua2, tuple(torch.empty_like(t) for t in (q, k, v, do)))]
     h_out = [[torch.empty(t.shape, dtype=torch.int16).pin_memory()
               for t in (ua.o, ua.dq, ua.dk, ua.dv)] for _ in range(2)]
@@ -406,9 +406,9 @@ def run_usp(args, wl, inp):
         value = aggregate_throughput(world, wl.S, args.steps, elapsed)
         t_fwd = stage_ms["attn_fwd"] / 1e3
         t_bwd = stage_ms["attn_bwd"] / 1e3
-        bq = wl.S_pad * wl.Hq * wl.D * 2
-        bkv = wl.S_pad * wl.Hkv * wl.D * 2
-        tab = wl.S_pad * wl.D * 4                  # one (cos, sin) row per position
+        bq = ua.S_pad * wl.Hq * wl.D * 2
+        bkv = ua.S_pad * wl.Hkv * wl.D * 2
+        tab = ua.S_pad * wl.D * 4                  # one (cos, sin) row per position
         rep_bytes = {"repack_qkv": 2 * (bq + 2 * bkv) + 2 * tab, "repack_o": 2 * bq,
                      "repack_do": 2 * bq, "repack_grads": 2 * (bq + 2 * bkv) + 2 * tab}
         rep_t = sum(stage_ms[n] for n in rep_bytes) / 1e3
@@ -424,6 +424,7 @@ def run_usp(args, wl, inp):
                        "D": wl.D, "rope": ("yarn x%g to %d" % (wl.yarn_factor, wl.rope_len)
                                            if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
                        "attention": "causal" if causal else "bidirectional",
+                       "shards": "zigzag" if args.zigzag else "contiguous",
                        "parallelism": f"replicas x{world} (P={wl.P} virtual shards per GPU)",
                        "l2": "inputs larger than L2 (Q alone %.2f GB); no flush" % (bq / 1e9)},
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
@@ -473,6 +474,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bidirectional", action="store_true",
                     help="attention over the whole document (causal = 0)")
+    ap.add_argument("--zigzag", action="store_true",
+                    help="zigzag shard layout (rank r holds chunks r and 2P-1-r of 2P)")
     args = ap.parse_args()
     from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, make_inputs
     wl = WORKLOADS[args.workload]
