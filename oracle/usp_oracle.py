@@ -366,6 +366,65 @@ def attention_fwd(q: np.ndarray, k: np.ndarray, v: np.ndarray, doc: np.ndarray,
     return o, lse
 
 
+# ---------------------------------------------------------------------------
+# Ring attention over R virtual ring ranks (SpecForge #728 configures a
+# Ulysses x Ring mesh, "Ulysses=8 / Ring=1" in its run; verl #45 builds a
+# (dp, ring, ulysses) mesh).  Reading: the key/value rows are cut into R
+# contiguous chunks; each ring step attends to one chunk and yields a
+# partial (O, LSE) normalised within that chunk; partials are merged with
+# the log-sum-exp combine  LSE = ln sum_i exp(LSE_i),
+# O = sum_i exp(LSE_i - LSE) O_i, which gives the attention over all chunks.
+# ---------------------------------------------------------------------------
+
+
+def attention_window(q, k, v, doc, scale, k_lo, k_hi, causal=True):
+    """Attention of every query row over the keys in rows [k_lo, k_hi) only
+    (mask as usual): q[T][Hq][D], k/v[T][Hkv][D] -> O[T][Hq][D], LSE[Hq][T]
+    (LSE -inf and O = 0 for a row with no visible key in the window)."""
+    T = q.shape[0]
+    inside = (np.arange(T) >= k_lo) & (np.arange(T) < k_hi)
+    doc_w = np.where(inside, doc, -2)          # keys outside the window match no row
+    o = np.zeros(q.shape)
+    lse = np.zeros((q.shape[1], T))
+    G = q.shape[1] // k.shape[1]
+    for h in range(q.shape[1]):
+        for a in range(0, T, _ROW_CHUNK):
+            rows = np.arange(a, min(T, a + _ROW_CHUNK))
+            sc = (q[rows, h] @ k[:, h // G].T) * scale
+            vis = _visible(rows, doc, causal) & (doc_w[None, :] == doc[rows][:, None])
+            sc = np.where(vis, sc, -np.inf)
+            m = sc.max(axis=1)
+            has = np.isfinite(m)
+            m_safe = np.where(has, m, 0.0)
+            e = np.exp(sc - m_safe[:, None])
+            l = e.sum(axis=1)
+            o[rows[has], h] = (e[has] @ v[:, h // G]) / l[has, None]
+            lse[h, rows] = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), -np.inf)
+    return o, lse
+
+
+def lse_merge(o_a, lse_a, o_b, lse_b):
+    """Log-sum-exp combine of two partial results (O[T][H][D], LSE[H][T])."""
+    lse = np.logaddexp(lse_a, lse_b)
+    fin = np.isfinite(lse)
+    w_a = np.where(fin, np.exp(np.where(fin, lse_a - np.where(fin, lse, 0.0), -np.inf)), 0.0)
+    w_b = np.where(fin, np.exp(np.where(fin, lse_b - np.where(fin, lse, 0.0), -np.inf)), 0.0)
+    o = o_a * w_a.T[:, :, None] + o_b * w_b.T[:, :, None]
+    return o, lse
+
+
+def ring_fwd(q, k, v, doc, scale, R, causal=True):
+    """Attention as R ring steps over contiguous key chunks, merged."""
+    T = q.shape[0]
+    L = -(-T // R)
+    o = np.zeros(q.shape)
+    lse = np.full((q.shape[1], T), -np.inf)
+    for c in range(R):
+        o_c, lse_c = attention_window(q, k, v, doc, scale, c * L, min(T, (c + 1) * L), causal)
+        o, lse = lse_merge(o, lse, o_c, lse_c)
+    return o, lse
+
+
 def attention_bwd_head(q, k, v, do, doc, scale, rows=None, causal=True):
     """Gradients of L = sum(O * dO) for one head (fp64, q/k/v/do [T][D]).
 
