@@ -163,6 +163,41 @@ usp_status usp_attn_fwd(const usp_dims* dims, const void* q_h, const void* k_h,
                         void* stream);
 
 /*
+ * usp_attn_fwd_window -- usp_attn_fwd over the keys in rows [k_lo, k_hi)
+ * only: one ring step of ring attention (SpecForge #728 runs a Ulysses x
+ * Ring mesh, "Ulysses=8 / Ring=1"; verl #45 builds a (dp, ring, ulysses)
+ * mesh).  M(t) of usp_attn_fwd is cut to k_lo <= u < k_hi; O is normalised
+ * within the window and LSE is the log-sum-exp over it (O = 0, LSE = -inf
+ * for a row that sees no key in the window).  Same arguments and errors as
+ * usp_attn_fwd, plus 0 <= k_lo <= k_hi <= S_pad (else USP_ERR_INVALID_ARG).
+ * Partial results of disjoint windows combine with usp_lse_merge into the
+ * attention over their union.
+ */
+usp_status usp_attn_fwd_window(const usp_dims* dims, const void* q_h, const void* k_h,
+                               const void* v_h, const int32_t* doc, int64_t k_lo,
+                               int64_t k_hi, void* o_h, float* lse, void* stream);
+
+/*
+ * usp_lse_merge -- merge one partial attention result into an accumulator
+ * (the log-sum-exp combine of ring attention):
+ *   LSE = ln(exp(LSE_acc) + exp(LSE_part)),
+ *   O   = exp(LSE_acc - LSE) O_acc + exp(LSE_part - LSE) O_part,
+ * a -inf term weighing 0 (both -inf: O = 0, LSE = -inf).
+ *   o_acc   [P][S_pad][Hq/P][D] fp32, in/out (ignored as input if first)
+ *   lse_acc [P][Hq/P][S_pad] fp32, in/out (ignored as input if first)
+ *   o_part  [P][S_pad][Hq/P][D] bf16, lse_part [P][Hq/P][S_pad] fp32: the
+ *           outputs of usp_attn_fwd_window
+ *   first   1: the accumulator is set to the partial result; 0: merged
+ *   o_out   NULL, or [P][S_pad][Hq/P][D] bf16 that receives the merged O
+ *           (the last step writes the forward's O this way; lse_acc is
+ *           then its LSE)
+ * All pointers 16-byte aligned.  fp32 arithmetic; deterministic.
+ */
+usp_status usp_lse_merge(const usp_dims* dims, float* o_acc, float* lse_acc,
+                         const void* o_part, const float* lse_part, int32_t first,
+                         void* o_out, void* stream);
+
+/*
  * usp_attn_bwd -- gradients of loss L with dL/dO = dO through usp_attn_fwd
  * (SpecForge #728, Accuracy Test: gradient parity with full-sequence
  * attention; verl #45: SP and non-SP fwd+bwd agree).

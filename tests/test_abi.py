@@ -66,6 +66,18 @@ def test_causal_flag_and_scale_checked():
     assert _fwd(d) == 1
 
 
+def test_window_and_merge_arguments_checked():
+    d = _dims()                                 # S_pad = 256
+    args = [ctypes.byref(d)] + [FAKE] * 4
+    for lo, hi in ((5, 4), (-1, 8), (0, 257)):
+        assert B.raw_call("usp_attn_fwd_window", *args, ctypes.c_int64(lo), ctypes.c_int64(hi),
+                          FAKE, FAKE, None) == 1
+    assert B.raw_call("usp_lse_merge", ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, 2, None,
+                      None) == 1
+    assert B.raw_call("usp_lse_merge", ctypes.byref(d), FAKE, None, FAKE, FAKE, 1, None,
+                      None) == 1
+
+
 def test_zigzag_pad_shard_cannot_run_in_place():
     d = _dims()
     d.zigzag = 1

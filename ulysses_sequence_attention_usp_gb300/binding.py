@@ -52,6 +52,8 @@ _SIGS = {
     "usp_pad_shard": [_DIMS, _P, _I32, _P, _P, _P, _P],
     "usp_seq_to_head_rope": [_DIMS, _P, _I32, _P, _P, _I64, _I32, _P, _P],
     "usp_attn_fwd": [_DIMS, _P, _P, _P, _P, _P, _P, _P],
+    "usp_attn_fwd_window": [_DIMS, _P, _P, _P, _P, _I64, _I64, _P, _P, _P],
+    "usp_lse_merge": [_DIMS, _P, _P, _P, _P, _I32, _P, _P],
     "usp_attn_bwd": [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "usp_attn_bwd_noalloc": [_DIMS, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "usp_head_to_seq": [_DIMS, _P, _I32, _P, _P, _I64, _I32, _P, _P],
@@ -138,6 +140,18 @@ def usp_seq_to_head_rope(dims, x_seq, H, pos, rope_cs, rope_len, rope_mode, x_he
 def usp_attn_fwd(dims, q_h, k_h, v_h, doc, o_h, lse, stream=None):
     _check(_lib.usp_attn_fwd(ctypes.byref(dims), _ptr(q_h), _ptr(k_h), _ptr(v_h), _ptr(doc),
                              _ptr(o_h), _ptr(lse), _stream(stream)), "usp_attn_fwd")
+
+
+def usp_attn_fwd_window(dims, q_h, k_h, v_h, doc, k_lo, k_hi, o_h, lse, stream=None):
+    _check(_lib.usp_attn_fwd_window(ctypes.byref(dims), _ptr(q_h), _ptr(k_h), _ptr(v_h),
+                                    _ptr(doc), int(k_lo), int(k_hi), _ptr(o_h), _ptr(lse),
+                                    _stream(stream)), "usp_attn_fwd_window")
+
+
+def usp_lse_merge(dims, o_acc, lse_acc, o_part, lse_part, first, o_out=None, stream=None):
+    _check(_lib.usp_lse_merge(ctypes.byref(dims), _ptr(o_acc), _ptr(lse_acc), _ptr(o_part),
+                              _ptr(lse_part), 1 if first else 0, _ptr(o_out), _stream(stream)),
+           "usp_lse_merge")
 
 
 def usp_attn_bwd_workspace(dims) -> int:

@@ -63,6 +63,7 @@ struct Params {
   int64_t S, S_pad;
   int hq, hkv, G, n_qtiles, slots_per_kv;
   int causal;             // 0: every key of the row's document is visible
+  int64_t k_lo, k_hi;     // key window: only rows [k_lo, k_hi) are keys
   float scale_log2;
   unsigned* status;
 };
@@ -164,10 +165,13 @@ __global__ void __launch_bounds__(384, 1)
   {
     const int64_t ds0 = doc_start_of(p, t0);
     if (ds0 >= 0) {
-      kv_start = (ds0 / BN) * BN;
       const int64_t last = min(t0 + BM, p.S) - 1;
-      const int64_t kv_end = p.causal ? last + 1 : doc_end_of(p, last);
-      n_kv = (int)((kv_end - kv_start + BN - 1) / BN);
+      const int64_t k0 = max(ds0, p.k_lo);
+      const int64_t kv_end = min(p.causal ? last + 1 : doc_end_of(p, last), p.k_hi);
+      if (kv_end > k0) {
+        kv_start = (k0 / BN) * BN;
+        n_kv = (int)((kv_end - kv_start + BN - 1) / BN);
+      }
     }
   }
 
@@ -297,8 +301,11 @@ __global__ void __launch_bounds__(384, 1)
     const int j = j0 + h;
     if (h < NH) {
       const int64_t ds = doc_start_of(p, t);    // -1: row sees nothing
-      // last visible key: the row itself (causal) or its document's last row
-      const int64_t ke = ds < 0 ? -1 : (p.causal ? t : doc_end_of(p, t) - 1);
+      // visible keys [ks, ke]: from the document start (or the window start)
+      // to the row itself (causal) or the document's last row, cut to the
+      // key window
+      const int64_t ks = max(ds, p.k_lo);
+      const int64_t ke = ds < 0 ? -1 : min(p.causal ? t : doc_end_of(p, t) - 1, p.k_hi - 1);
       const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, C::S_COL(h));
       const uint32_t tO = tc::tmem_addr(tmem, quarter * 32, C::O_COL(h));
       float m = -INFINITY, l = 0.f;
@@ -308,10 +315,10 @@ __global__ void __launch_bounds__(384, 1)
         if (!ok) break;
         tc::fence_after_sync();
         const int64_t u0 = kv_start + (int64_t)jt * BN;
-        const bool row_mask = ds < 0 || u0 < ds || u0 + BN - 1 > ke;
+        const bool row_mask = ds < 0 || u0 < ks || u0 + BN - 1 > ke;
         const bool mask = __any_sync(0xffffffffu, row_mask);
-        // keys u0+c visible to row t iff ds <= u0+c <= ke  (c in [lo, hi])
-        const int lo = (int)max((int64_t)0, min((int64_t)BN, ds - u0));
+        // keys u0+c visible to row t iff ks <= u0+c <= ke  (c in [lo, hi])
+        const int lo = (int)max((int64_t)0, min((int64_t)BN, ks - u0));
         const int hi = ds < 0 ? -1 : (int)max((int64_t)-1, min((int64_t)BN - 1, ke - u0));
         // the mask is warp-uniform, so fully visible tiles take the path
         // without per-column tests
@@ -438,7 +445,8 @@ cudaError_t launch_fwd(const usp::Geometry& g, const CUtensorMap& mq, const CUte
 
 cudaError_t usp_launch_attn_fwd(const usp::Geometry& g, const void* q, const void* k,
                                 const void* v, const int32_t* doc, const int32_t* cu,
-                                void* o, float* lse, cudaStream_t st) {
+                                void* o, float* lse, cudaStream_t st, int64_t k_lo,
+                                int64_t k_hi) {
   CUtensorMap mq, mk, mv;
   if (!usp_make_head_map(&mq, q, g.hq, g.D, g.S_pad, g.P, 128) ||
       !usp_make_head_map(&mk, k, g.hkv, g.D, g.S_pad, g.P, 128) ||
@@ -458,6 +466,8 @@ cudaError_t usp_launch_attn_fwd(const usp::Geometry& g, const void* q, const voi
   prm.n_qtiles = (int)((g.S_pad + BM - 1) / BM);
   prm.slots_per_kv = g.G / nh;
   prm.causal = g.causal;
+  prm.k_lo = k_lo;
+  prm.k_hi = k_hi;
   prm.scale_log2 = g.scale * kLog2e;
   prm.status = g.status;
   if (g.D == 128)

@@ -165,9 +165,9 @@ usp_status usp_head_to_seq(const usp_dims* dims, const void* x_head, int32_t H,
   return repack(dims, x_head, H, pos, rope_cs, rope_len, rope_mode, x_seq, false, stream);
 }
 
-usp_status usp_attn_fwd(const usp_dims* dims, const void* q_h, const void* k_h,
-                        const void* v_h, const int32_t* doc, void* o_h, float* lse,
-                        void* stream) {
+static usp_status attn_fwd(const usp_dims* dims, const void* q_h, const void* k_h,
+                           const void* v_h, const int32_t* doc, int64_t k_lo, int64_t k_hi,
+                           bool window, void* o_h, float* lse, void* stream) {
   usp::Geometry g;
   usp_status s = geometry(dims, &g);
   if (s != USP_OK) return s;
@@ -175,10 +175,43 @@ usp_status usp_attn_fwd(const usp_dims* dims, const void* q_h, const void* k_h,
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return USP_ERR_INVALID_ARG;
   if (doc == nullptr || ((uintptr_t)doc & 3u)) return USP_ERR_INVALID_ARG;
+  if (!window) {
+    k_lo = 0;
+    k_hi = g.S_pad;
+  } else if (k_lo < 0 || k_lo > k_hi || k_hi > g.S_pad) {
+    return USP_ERR_INVALID_ARG;
+  }
   if (g.S_pad == 0) return USP_OK;
   if ((g.status = status_word()) == nullptr) return USP_ERR_CUDA;
   return cuda_status(usp_launch_attn_fwd(g, q_h, k_h, v_h, doc, dims->cu_seqlens, o_h, lse,
-                                         (cudaStream_t)stream));
+                                         (cudaStream_t)stream, k_lo, k_hi));
+}
+
+usp_status usp_attn_fwd(const usp_dims* dims, const void* q_h, const void* k_h,
+                        const void* v_h, const int32_t* doc, void* o_h, float* lse,
+                        void* stream) {
+  return attn_fwd(dims, q_h, k_h, v_h, doc, 0, 0, false, o_h, lse, stream);
+}
+
+usp_status usp_attn_fwd_window(const usp_dims* dims, const void* q_h, const void* k_h,
+                               const void* v_h, const int32_t* doc, int64_t k_lo, int64_t k_hi,
+                               void* o_h, float* lse, void* stream) {
+  return attn_fwd(dims, q_h, k_h, v_h, doc, k_lo, k_hi, true, o_h, lse, stream);
+}
+
+usp_status usp_lse_merge(const usp_dims* dims, float* o_acc, float* lse_acc, const void* o_part,
+                         const float* lse_part, int32_t first, void* o_out, void* stream) {
+  usp::Geometry g;
+  usp_status s = geometry(dims, &g);
+  if (s != USP_OK) return s;
+  const void* ptrs[] = {o_acc, lse_acc, o_part, lse_part};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return USP_ERR_INVALID_ARG;
+  if (o_out != nullptr && !aligned16(o_out)) return USP_ERR_INVALID_ARG;
+  if (first != 0 && first != 1) return USP_ERR_INVALID_ARG;
+  if (g.S_pad == 0) return USP_OK;
+  return cuda_status(usp_launch_lse_merge(g, o_acc, lse_acc, o_part, lse_part, first, o_out,
+                                          (cudaStream_t)stream));
 }
 
 size_t usp_attn_bwd_workspace(const usp_dims* dims) {

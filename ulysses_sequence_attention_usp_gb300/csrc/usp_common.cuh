@@ -44,7 +44,11 @@ cudaError_t usp_launch_repack(const usp::Geometry& g, const void* src, int H, co
                               bool to_head, void* dst, cudaStream_t st);
 cudaError_t usp_launch_attn_fwd(const usp::Geometry& g, const void* q, const void* k,
                                 const void* v, const int32_t* doc, const int32_t* cu,
-                                void* o, float* lse, cudaStream_t st);
+                                void* o, float* lse, cudaStream_t st, int64_t k_lo,
+                                int64_t k_hi);
+cudaError_t usp_launch_lse_merge(const usp::Geometry& g, float* o_acc, float* lse_acc,
+                                 const void* o_part, const float* lse_part, int first,
+                                 void* o_out, cudaStream_t st);
 cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const void* k,
                                 const void* v, const void* o, const float* lse,
                                 const void* dout, const int32_t* doc, const int32_t* cu,

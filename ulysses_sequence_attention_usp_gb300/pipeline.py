@@ -24,11 +24,14 @@ from . import binding as B
 class UlyssesAttention:
     def __init__(self, S, P, Hq, Hkv, D, cu_seqlens=None, rope_base=1.0e4, yarn_factor=1.0,
                  yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None,
-                 causal=True, zigzag=False):
+                 causal=True, zigzag=False, ring=1):
         self.S, self.P, self.Hq, self.Hkv, self.D = int(S), int(P), int(Hq), int(Hkv), int(D)
         unit = 2 * self.P if zigzag else self.P      # zigzag: 2P equal chunks
         self.S_pad = -(-self.S // unit) * unit
         self.zigzag = bool(zigzag)
+        self.ring = int(ring)
+        if self.ring < 1:
+            raise ValueError("ring must be >= 1")
         self.device = torch.device(device)
         dev = self.device
         self.cu_host = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, np.int32)
@@ -56,6 +59,10 @@ class UlyssesAttention:
         self.dk, self.dv = e(Sp, Hkv, D), e(Sp, Hkv, D)
         self.ws_bytes = B.usp_attn_bwd_workspace(self.dims)
         self.ws = e(max(1, self.ws_bytes), dt=torch.uint8)
+        if self.ring > 1:   # partial results of one ring step and the fp32 accumulator
+            self.o_part = e(P, Sp, hq, D)
+            self.lse_part = e(P, hq, Sp, dt=torch.float32)
+            self.o_acc = e(P, Sp, hq, D, dt=torch.float32)
 
     # -- steps -------------------------------------------------------------
     def forward(self, q, k, v, stream=None):
@@ -71,7 +78,19 @@ class UlyssesAttention:
         B.usp_seq_to_head_rope(d, self.k_seq, self.Hkv, self.pos, self.rope, self.rope_len, 1,
                                self.k_h, st)
         B.usp_seq_to_head_rope(d, self.v_seq, self.Hkv, None, None, 0, 0, self.v_h, st)
-        B.usp_attn_fwd(d, self.q_h, self.k_h, self.v_h, self.doc, self.o_h, self.lse, st)
+        if self.ring == 1:
+            B.usp_attn_fwd(d, self.q_h, self.k_h, self.v_h, self.doc, self.o_h, self.lse, st)
+        else:
+            # ring attention: step c attends to key rows [c*L, (c+1)*L); the
+            # partial results are merged (log-sum-exp) into an fp32
+            # accumulator, and the last merge writes O and its LSE
+            L = -(-self.S_pad // self.ring)
+            for c in range(self.ring):
+                lo, hi = min(self.S_pad, c * L), min(self.S_pad, (c + 1) * L)
+                B.usp_attn_fwd_window(d, self.q_h, self.k_h, self.v_h, self.doc, lo, hi,
+                                      self.o_part, self.lse_part, st)
+                B.usp_lse_merge(d, self.o_acc, self.lse, self.o_part, self.lse_part, c == 0,
+                                self.o_h if c == self.ring - 1 else None, st)
         B.usp_head_to_seq(d, self.o_h, self.Hq, None, None, 0, 0, self.o, st)
         return self.o
 
