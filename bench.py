@@ -272,7 +272,7 @@ def run_usp(args, wl, inp):
     ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
                           rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
                           yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
-                          causal=causal, zigzag=args.zigzag)
+                          causal=causal, zigzag=args.zigzag, ring=args.ring)
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     st = torch.cuda.current_stream(dev)
     d = ua.dims
@@ -292,7 +292,7 @@ def run_usp(args, wl, inp):
         B.usp_seq_to_head_rope(d, ua.k_seq, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1, ua.k_h, st)
         B.usp_seq_to_head_rope(d, ua.v_seq, wl.Hkv, None, None, 0, 0, ua.v_h, st)
         mark(2)
-        B.usp_attn_fwd(d, ua.q_h, ua.k_h, ua.v_h, ua.doc, ua.o_h, ua.lse, st)
+        ua.attention_forward(st)           # one launch, or the ring steps
         mark(3)
         B.usp_head_to_seq(d, ua.o_h, wl.Hq, None, None, 0, 0, ua.o, st)
         mark(4)
@@ -348,7 +348,8 @@ def run_usp(args, wl, inp):
     ua2 = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
                            rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
                            yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
-                           rope_table=ua.rope_host, causal=causal, zigzag=args.zigzag)
+                           rope_table=ua.rope_host, causal=causal, zigzag=args.zigzag,
+                           ring=args.ring)
     pipes = [(ua, (q, k, v, do)), (ua2, tuple(torch.empty_like(t) for t in (q, k, v, do)))]
     h_out = [[torch.empty(t.shape, dtype=torch.int16).pin_memory()
               for t in (ua.o, ua.dq, ua.dk, ua.dv)] for _ in range(2)]
@@ -425,6 +426,7 @@ def run_usp(args, wl, inp):
                                            if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
                        "attention": "causal" if causal else "bidirectional",
                        "shards": "zigzag" if args.zigzag else "contiguous",
+                       "ring": args.ring,
                        "parallelism": f"replicas x{world} (P={wl.P} virtual shards per GPU)",
                        "l2": "inputs larger than L2 (Q alone %.2f GB); no flush" % (bq / 1e9)},
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
@@ -476,6 +478,8 @@ def main():
                     help="attention over the whole document (causal = 0)")
     ap.add_argument("--zigzag", action="store_true",
                     help="zigzag shard layout (rank r holds chunks r and 2P-1-r of 2P)")
+    ap.add_argument("--ring", type=int, default=1,
+                    help="ring steps of the forward (key windows merged by log-sum-exp)")
     args = ap.parse_args()
     from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, make_inputs
     wl = WORKLOADS[args.workload]

@@ -78,21 +78,29 @@ class UlyssesAttention:
         B.usp_seq_to_head_rope(d, self.k_seq, self.Hkv, self.pos, self.rope, self.rope_len, 1,
                                self.k_h, st)
         B.usp_seq_to_head_rope(d, self.v_seq, self.Hkv, None, None, 0, 0, self.v_h, st)
-        if self.ring == 1:
-            B.usp_attn_fwd(d, self.q_h, self.k_h, self.v_h, self.doc, self.o_h, self.lse, st)
-        else:
-            # ring attention: step c attends to key rows [c*L, (c+1)*L); the
-            # partial results are merged (log-sum-exp) into an fp32
-            # accumulator, and the last merge writes O and its LSE
-            L = -(-self.S_pad // self.ring)
-            for c in range(self.ring):
-                lo, hi = min(self.S_pad, c * L), min(self.S_pad, (c + 1) * L)
-                B.usp_attn_fwd_window(d, self.q_h, self.k_h, self.v_h, self.doc, lo, hi,
-                                      self.o_part, self.lse_part, st)
-                B.usp_lse_merge(d, self.o_acc, self.lse, self.o_part, self.lse_part, c == 0,
-                                self.o_h if c == self.ring - 1 else None, st)
+        self.attention_forward(st)
         B.usp_head_to_seq(d, self.o_h, self.Hq, None, None, 0, 0, self.o, st)
         return self.o
+
+    def attention_forward(self, stream=None):
+        """The attention of the head-layout Q, K, V into o_h and lse: one call,
+        or with ring > 1 the ring steps -- step c attends to key rows
+        [c*L, (c+1)*L), the partial results are merged (log-sum-exp) into an
+        fp32 accumulator, and the last merge writes O and its LSE.  The
+        backward then runs on the merged O and LSE: with every key chunk
+        resident, the ring backward's per-block sums equal the key- and
+        query-stationary passes over the whole range."""
+        d, st = self.dims, stream
+        if self.ring == 1:
+            B.usp_attn_fwd(d, self.q_h, self.k_h, self.v_h, self.doc, self.o_h, self.lse, st)
+            return
+        L = -(-self.S_pad // self.ring)
+        for c in range(self.ring):
+            lo, hi = min(self.S_pad, c * L), min(self.S_pad, (c + 1) * L)
+            B.usp_attn_fwd_window(d, self.q_h, self.k_h, self.v_h, self.doc, lo, hi,
+                                  self.o_part, self.lse_part, st)
+            B.usp_lse_merge(d, self.o_acc, self.lse, self.o_part, self.lse_part, c == 0,
+                            self.o_h if c == self.ring - 1 else None, st)
 
     def backward(self, do, stream=None):
         """do [S][Hq][D] bf16 (dL/dO).  Returns dQ, dK, dV [S_pad][H][D]: the
