@@ -122,11 +122,12 @@ __device__ __forceinline__ float softmax_row(uint32_t tS, int lo, int hi, float 
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float p0 = tc::ex2(fmaf(__uint_as_float(v[c * 32 + 2 * i]), sl2, -m_eff));
-      const float p1 = tc::ex2(fmaf(__uint_as_float(v[c * 32 + 2 * i + 1]), sl2, -m_eff));
-      r0 += p0;
-      r1 += p1;
+    for (int i = 0; i < 16; ++i) {   // pairs: one packed fma and one packed add
+      float x0, x1;
+      tc::fma2(x0, x1, __uint_as_float(v[c * 32 + 2 * i]), __uint_as_float(v[c * 32 + 2 * i + 1]),
+               sl2, sl2, -m_eff, -m_eff);
+      const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+      tc::add2(r0, r1, r0, r1, p0, p1);
       w[i] = tc::pack_bf16(p0, p1);
     }
     tc::tmem_st_x16(tS + c * 16, w);
