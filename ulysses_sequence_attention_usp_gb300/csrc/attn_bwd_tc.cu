@@ -85,8 +85,10 @@ struct Params {
   const int32_t* doc;
   const int32_t* cu;
   const bf16* q;         // head-layout Q (the dQ pass keeps its Q tile in TMEM)
-  const float* lse2;     // [P][hq][S_ws] LSE*log2(e); +inf for rows without keys
-  const float* delta;    // [P][hq][S_ws] rowsum(dO*O); S_ws = S_pad rounded up to BT
+  // both negated so that the elementwise code adds them with packed pair
+  // instructions, which take no operand negation
+  const float* nlse2;    // [P][hq][S_ws] -LSE*log2(e); -inf for rows without keys
+  const float* ndelta;   // [P][hq][S_ws] -rowsum(dO*O); S_ws = S_pad rounded up to BT
   bf16* dq;
   bf16* dk;
   bf16* dv;
@@ -338,7 +340,9 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
 //            written as bf16 over dP^T.
 // dS^T is thus formed from the bf16 P^T that dV is built from (a relative
 // change of at most 2^-9 per element, the size of the rounding dS^T gets
-// anyway).  The per-column lse2 and delta come in registers.
+// anyway).  The per-column lse2 and delta come in registers, negated (the
+// workspace stores -lse2 and -delta), and pairs of columns go through packed
+// fp32x2 instructions.
 // bf16 values of each 32-column chunk go to that chunk's first 16 columns.
 // Columns outside [lo, hi] are zero when MASK.
 template <bool MASK>
@@ -350,14 +354,16 @@ __device__ __forceinline__ void dkdv_phase_p(uint32_t tS, int h, int lo, int hi,
     tc::tmem_ld_x32(tS + 64 * h + 32 * cc, sv);
     uint32_t pw[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 16; ++i) {   // pairs of columns: one packed fma per pair
       float pv[2];
+      const int k = 32 * cc + 2 * i;
+      tc::fma2(pv[0], pv[1], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2,
+               sl2, l2[k], l2[k + 1]);   // l2 holds -LSE*log2(e)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int k = 32 * cc + 2 * i + e;
-        pv[e] = tc::ex2(fmaf(__uint_as_float(sv[2 * i + e]), sl2, -l2[k]));
+        pv[e] = tc::ex2(pv[e]);
         if (MASK) {
-          const int col = 64 * h + k;
+          const int col = 64 * h + k + e;
           if (!(col >= lo && col <= hi)) pv[e] = 0.f;
         }
       }
@@ -380,8 +386,11 @@ __device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, int h, const float (&
       const uint32_t w = pk[16 * cc + i];
       const float p0 = __uint_as_float(w << 16), p1 = __uint_as_float(w & 0xffff0000u);
       const int k = 32 * cc + 2 * i;
-      dw[i] = tc::pack_bf16(p0 * (__uint_as_float(dv[2 * i]) - d2[k]),
-                            p1 * (__uint_as_float(dv[2 * i + 1]) - d2[k + 1]));
+      float t0, t1;   // (dP^T - delta) P^T with d2 holding -delta, as packed pairs
+      tc::add2(t0, t1, __uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]), d2[k],
+               d2[k + 1]);
+      tc::mul2(t0, t1, p0, p1, t0, t1);
+      dw[i] = tc::pack_bf16(t0, t1);
     }
     tc::tmem_st_x16(tP + 64 * h + 32 * cc, dw);
   }
@@ -401,11 +410,12 @@ __device__ __forceinline__ void load_vec64(const float* src, float (&v)[64]) {
 
 // dQ elementwise work on half h (keys [64h, 64h+64)) of this thread's query
 // row: read S and dP, let the MMA issuer reuse them ("consumed"), compute
-// dS = exp2(S*sl2 - lse2) (dP - delta) and, once the dS columns are free,
+// dS = exp2(S*sl2 - lse2) (dP - delta) (with nlse2 = -lse2 and ndl = -delta,
+// as packed pairs) and, once the dS columns are free,
 // write it there as bf16 (32 columns: K steps 4h..4h+3).
 template <bool MASK>
 __device__ __forceinline__ bool dq_half(uint32_t tS, uint32_t tP, uint32_t tR, int h, int lo,
-                                        int hi, float lse2, float dl, float sl2, Bars* bars,
+                                        int hi, float nlse2, float ndl, float sl2, Bars* bars,
                                         int j, volatile int* abort) {
   uint32_t sv[64], dv[64];
   tc::tmem_ld2_x64(tS + 64 * h, tP + 64 * h, sv, dv);
@@ -414,17 +424,18 @@ __device__ __forceinline__ bool dq_half(uint32_t tS, uint32_t tP, uint32_t tR, i
   uint32_t w[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
+    float x0, x1, t0, t1;
+    tc::fma2(x0, x1, __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]), sl2, sl2, nlse2,
+             nlse2);
+    tc::add2(t0, t1, __uint_as_float(dv[2 * i]), __uint_as_float(dv[2 * i + 1]), ndl, ndl);
     float dd[2];
+    tc::mul2(dd[0], dd[1], tc::ex2(x0), tc::ex2(x1), t0, t1);
+    if (MASK) {
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int k = 2 * i + e;
-      const float pv = tc::ex2(fmaf(__uint_as_float(sv[k]), sl2, -lse2));
-      float dsv = pv * (__uint_as_float(dv[k]) - dl);
-      if (MASK) {
-        const int col = 64 * h + k;
-        if (!(col >= lo && col <= hi)) dsv = 0.f;
+      for (int e = 0; e < 2; ++e) {
+        const int col = 64 * h + 2 * i + e;
+        if (!(col >= lo && col <= hi)) dd[e] = 0.f;
       }
-      dd[e] = dsv;
     }
     w[i] = tc::pack_bf16(dd[0], dd[1]);
   }
@@ -504,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // lse2 next to the Q tile, delta next to the dO tile
             const int64_t off = ((int64_t)g * p.hq + jk * G + it % G) * p.S_ws + tq0 +
                                 (int64_t)(it / G) * BT;
-            return (w == 0 ? p.lse2 : p.delta) + off;
+            return (w == 0 ? p.nlse2 : p.ndelta) + off;
           });
     }
   } else if (warp == 1) {
@@ -653,11 +664,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t ds = doc_start_of(p, t);
     // last key row t sees: itself (causal) or its document's last row
     const int64_t ke = ds < 0 ? -1 : (p.causal ? t : doc_end_of(p, t) - 1);
-    float lse2 = INFINITY, dl = 0.f;
+    float nlse2 = -INFINITY, ndl = 0.f;
     if (ds >= 0) {
       const int64_t li = ((int64_t)g * p.hq + jq) * p.S_ws + t;
-      lse2 = __ldg(p.lse2 + li);
-      dl = __ldg(p.delta + li);
+      nlse2 = __ldg(p.nlse2 + li);
+      ndl = __ldg(p.ndelta + li);
     }
     const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, kDqT0);
     const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, kDqT1);
@@ -690,8 +701,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int hi = ds < 0 ? -1 : (int)max((int64_t)-1, min((int64_t)BT - 1, ke - u0));
       const bool mask = __any_sync(0xffffffffu, lo > 64 * half || hi < 64 * half + 63);
       const uint32_t tRb = tR;
-      ok = mask ? dq_half<true>(tS, tP, tRb, half, lo, hi, lse2, dl, p.scale_log2, bars, it, abort)
-                : dq_half<false>(tS, tP, tRb, half, lo, hi, lse2, dl, p.scale_log2, bars, it, abort);
+      ok = mask ? dq_half<true>(tS, tP, tRb, half, lo, hi, nlse2, ndl, p.scale_log2, bars, it,
+                                abort)
+                : dq_half<false>(tS, tP, tRb, half, lo, hi, nlse2, ndl, p.scale_log2, bars, it,
+                                 abort);
       if (!ok) break;
       tc::tmem_wait_st();
       tc::fence_before_sync();
@@ -727,8 +740,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------ delta = rowsum(dO*O)
 // One warp per (row, head): 16-byte loads, fp32 products and a shuffle sum.
-// Also writes lse2 = LSE*log2(e) (+inf where LSE = -inf).  Both arrays have
-// rows of S_ws >= S_pad entries; entries [S_pad, S_ws) get delta 0, lse2 +inf.
+// Writes both negated: ndelta = -delta and nlse2 = -LSE*log2(e) (-inf where
+// LSE = -inf).  Both arrays have rows of S_ws >= S_pad entries; entries
+// [S_pad, S_ws) get ndelta 0 and nlse2 -inf.
 template <int D>
 __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
                                                     const bf16* __restrict__ dout,
@@ -744,7 +758,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
       const int64_t rr = i / extra;
       const int64_t idx = rr * S_ws + S_pad + (i - rr * extra);
       delta[idx] = 0.f;
-      lse2[idx] = INFINITY;
+      lse2[idx] = -INFINITY;
     }
   }
   constexpr int LPR = D / 8;                  // lanes per row (8 bf16 each)
@@ -775,9 +789,9 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
       const int j = (int)(row - gt * hq);
       const int64_t g = gt / S_pad, t = gt - g * S_pad;
       const int64_t li = (g * hq + j) * S_ws + t;
-      delta[li] = s;
+      delta[li] = -s;
       const float x = lse[(g * hq + j) * S_pad + t];
-      lse2[li] = x == -INFINITY ? INFINITY : x * kLog2e;
+      lse2[li] = x == -INFINITY ? -INFINITY : -(x * kLog2e);
     }
   }
 }
@@ -838,8 +852,8 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
   prm.q = reinterpret_cast<const bf16*>(q);
   float* delta = reinterpret_cast<float*>(ws);
   float* lse2 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + vec_bytes(g));
-  prm.lse2 = lse2;
-  prm.delta = delta;
+  prm.nlse2 = lse2;
+  prm.ndelta = delta;
   prm.dq = reinterpret_cast<bf16*>(dq);
   prm.dk = reinterpret_cast<bf16*>(dk);
   prm.dv = reinterpret_cast<bf16*>(dv);
