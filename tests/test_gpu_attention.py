@@ -35,6 +35,8 @@ SMALL = [  # S, P, Hq, Hkv, D, doc lengths (None = one sequence)
     (30, 4, 8, 4, 128, None),             # padded 30 -> 32
     (1, 8, 8, 8, 128, None),              # one token, fewer rows than ranks
     (600, 2, 16, 2, 128, [200, 400]),     # G = 8 as in the packed 64/8 workload
+    (300, 2, 8, 2, 128, [100, 0, 150, 0, 50]),  # empty documents in cu_seqlens
+    (512, 1, 4, 2, 64, [200, 312]),       # one rank (P = 1): no head split
 ]
 
 
