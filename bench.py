@@ -7,7 +7,9 @@ A step is one full pass of the path over one synthetic batch:
   -> head->seq (dQ, dK with inverse RoPE; dV).
 The default workload is the 120 000-token SP8 layer (Hq/Hkv/D = 32/8/128,
 YaRN RoPE to 131 072).  Inputs (0.98 GB for Q alone) are larger than L2, so
-no flush is needed between steps.
+no flush is needed between steps.  The permutation stages' GB/s is taken
+from a separate leg that runs each stage alone after a memset of twice the
+L2 size.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU fp64 oracle, timed
@@ -34,6 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "USP attn fwd+bwd tokens/s and TFLOP/s (% bf16 peak); repack GB/s (% HBM)"
+FLUSH_ITERS = 10        # timed calls of each permutation stage after an L2 flush
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -337,6 +340,40 @@ def run_usp(args, wl, inp):
                 for j, n in enumerate(stage_names)}
     elapsed = reduce_max(elapsed, world, dev)
 
+    # ---- the permutation stages alone, each preceded by a memset of twice
+    # the L2 size so that none of its inputs is L2-resident: their GB/s is
+    # then HBM bandwidth.  Median of FLUSH_ITERS calls of each stage.
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    rep_calls = {
+        "repack_qkv": lambda: (
+            B.usp_seq_to_head_rope(d, ua.q_seq, wl.Hq, ua.pos, ua.rope, ua.rope_len, 1, ua.q_h, st),
+            B.usp_seq_to_head_rope(d, ua.k_seq, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1, ua.k_h, st),
+            B.usp_seq_to_head_rope(d, ua.v_seq, wl.Hkv, None, None, 0, 0, ua.v_h, st)),
+        "repack_o": lambda: B.usp_head_to_seq(d, ua.o_h, wl.Hq, None, None, 0, 0, ua.o, st),
+        "repack_do": lambda: B.usp_seq_to_head_rope(d, ua.do_seq, wl.Hq, None, None, 0, 0,
+                                                    ua.do_h, st),
+        "repack_grads": lambda: (
+            B.usp_head_to_seq(d, ua.dq_h, wl.Hq, ua.pos, ua.rope, ua.rope_len, -1, ua.dq, st),
+            B.usp_head_to_seq(d, ua.dk_h, wl.Hkv, ua.pos, ua.rope, ua.rope_len, -1, ua.dk, st),
+            B.usp_head_to_seq(d, ua.dv_h, wl.Hkv, None, None, 0, 0, ua.dv, st)),
+    }
+    flushed_ms = {}
+    with torch.cuda.stream(st):
+        for name, call in rep_calls.items():
+            times = []
+            for _ in range(FLUSH_ITERS):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                call()
+                e1.record(st)
+                times.append((e0, e1))
+            st.synchronize()
+            flushed_ms[name] = statistics.median(a.elapsed_time(b) for a, b in times)
+    ua.check(st)
+    del flush
+
     # ---- end to end through the public API with host buffers.  Every step
     # copies its inputs host->device (one copy stream), runs the step (`st`)
     # and copies its O, dQ, dK, dV device->host (another copy stream).  Two
@@ -425,7 +462,10 @@ def run_usp(args, wl, inp):
         rep_bytes = {"repack_qkv": 2 * (bq + 2 * bkv) + 2 * tab, "repack_o": 2 * bq,
                      "repack_do": 2 * bq, "repack_grads": 2 * (bq + 2 * bkv) + 2 * tab}
         rep_t = sum(stage_ms[n] for n in rep_bytes) / 1e3
-        rep_gbs = sum(rep_bytes.values()) / rep_t / 1e9
+        rep_gbs_step = sum(rep_bytes.values()) / rep_t / 1e9
+        rep_tf = sum(flushed_ms[n] for n in rep_bytes) / 1e3
+        rep_gbs = sum(rep_bytes.values()) / rep_tf / 1e9
+        f_bwd_strict = 8.0 * wl.D * wl.Hq * pairs
         peak_t = peaks["bf16_tflops_sustained"]
         bwd_tf = f_bwd / t_bwd / 1e12
         line = {
@@ -440,7 +480,9 @@ def run_usp(args, wl, inp):
                        "shards": "zigzag" if args.zigzag else "contiguous",
                        "ring": args.ring,
                        "parallelism": f"replicas x{world} (P={wl.P} virtual shards per GPU)",
-                       "l2": "inputs larger than L2 (Q alone %.2f GB); no flush" % (bq / 1e9)},
+                       "l2": ("step: inputs larger than L2 (Q alone %.2f GB), no flush; "
+                              "repack GB/s: each stage timed alone after a %d MB memset"
+                              % (bq / 1e9, 2 * l2 >> 20))},
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
                          "bound": "tensor", "achieved": bwd_tf,
                          "peak": peak_t, "unit": "TFLOP/s", "frac": bwd_tf / peak_t,
@@ -450,11 +492,17 @@ def run_usp(args, wl, inp):
             "attention": {"fwd_tflops": f_fwd / t_fwd / 1e12, "bwd_tflops": bwd_tf,
                           "fwd_frac": f_fwd / t_fwd / 1e12 / peak_t,
                           "fwd_bwd_tflops": (f_fwd + f_bwd) / (t_fwd + t_bwd) / 1e12,
+                          "bwd_tflops_strict": f_bwd_strict / t_bwd / 1e12,
+                          "bwd_flops": {"convention_2.5x": f_bwd, "strict_no_recompute": f_bwd_strict},
                           "fwd_ms": t_fwd * 1e3, "bwd_ms": t_bwd * 1e3,
                           "attended_pairs": pairs},
             "repack": {"gbps": rep_gbs, "frac": rep_gbs / peaks["hbm_gbs"],
                        "peak_gbps": peaks["hbm_gbs"], "peak_source": src,
-                       "bytes_per_step": sum(rep_bytes.values())},
+                       "bytes_per_step": sum(rep_bytes.values()),
+                       "timing": "each stage alone, L2 flushed before each call, "
+                                 "median of %d" % FLUSH_ITERS,
+                       "stage_ms_l2_flushed": flushed_ms,
+                       "gbps_in_step": rep_gbs_step},
             "stage_ms": stage_ms,
             "gpu_launches": launches,
             "e2e": {"value": aggregate_throughput(world, wl.S, e2e_steps, e2e_t), "unit": "tokens/s",
