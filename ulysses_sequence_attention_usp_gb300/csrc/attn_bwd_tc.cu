@@ -94,6 +94,7 @@ struct Params {
   bf16* dv;
   int64_t S, S_pad, S_ws;
   int hq, hkv, G, n_tiles;
+  int band_kv, band_q;   // head slots per band of the dkdv / dq CTA order (usp::cta_coords)
   int causal;            // 0: every key of a row's document is visible
   float scale, scale_log2;
   unsigned* status;
@@ -473,9 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int64_t u0 = (int64_t)blockIdx.x * BT;
-  const int g = blockIdx.y / p.hkv;
-  const int jk = blockIdx.y % p.hkv;
+  // rank 0 = key tile 0, which every causal query sees (the heaviest)
+  int rank, y;
+  usp::cta_coords(p.n_tiles, p.band_kv, rank, y);
+  const int64_t u0 = (int64_t)rank * BT;
+  const int g = y / p.hkv;
+  const int jk = y % p.hkv;
   // query rows that see these keys: from u0 (causal) or the first key's
   // document start, to the end of the last valid key's document
   int n_q = 0;
@@ -615,10 +619,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int qt = p.n_tiles - 1 - (int)blockIdx.x;
+  // rank 0 = the last query tile, the heaviest causal one
+  int rank, y;
+  usp::cta_coords(p.n_tiles, p.band_q, rank, y);
+  const int qt = p.n_tiles - 1 - rank;
   const int64_t t0 = (int64_t)qt * BT;
-  const int g = blockIdx.y / p.hq;
-  const int jq = blockIdx.y % p.hq;
+  const int g = y / p.hq;
+  const int jq = y % p.hq;
   const int jk = jq / p.G;
   int n_kv = 0;
   int64_t kv_start = 0;
@@ -801,6 +808,9 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
                        const CUtensorMap& mv, const CUtensorMap& mdo, const Params& prm,
                        const bf16* o, const bf16* dout, const float* lse, float* delta,
                        float* lse2, cudaStream_t st) {
+  const int64_t n_kv_cta = (int64_t)prm.n_tiles * g.P * g.hkv;
+  const int64_t n_q_cta = (int64_t)prm.n_tiles * g.P * g.hq;
+  if (n_q_cta > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const int64_t n_rows = (int64_t)g.P * g.S_pad * g.hq;
   int64_t blocks = (n_rows * (D / 8) * 1 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
@@ -816,11 +826,9 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
   if ((e = cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem_q)) != cudaSuccess)
     return e;
-  dkdv_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hkv)), kThreads, smem_kv, st>>>(
-      mq, mk, mv, mdo, prm);
+  dkdv_kernel<D><<<(unsigned)n_kv_cta, kThreads, smem_kv, st>>>(mq, mk, mv, mdo, prm);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  dq_kernel<D><<<dim3((unsigned)prm.n_tiles, (unsigned)(g.P * g.hq)), kThreads, smem_q, st>>>(
-      mq, mk, mv, mdo, prm);
+  dq_kernel<D><<<(unsigned)n_q_cta, kThreads, smem_q, st>>>(mq, mk, mv, mdo, prm);
   usp_count_launches(3);
   return cudaGetLastError();
 }
@@ -865,6 +873,8 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
   prm.G = g.G;
   prm.causal = g.causal;
   prm.n_tiles = (int)((g.S_pad + BT - 1) / BT);
+  prm.band_kv = usp::cta_band(prm.n_tiles, g.P * g.hkv);
+  prm.band_q = usp::cta_band(prm.n_tiles, g.P * g.hq);
   prm.scale = g.scale;
   prm.scale_log2 = g.scale * kLog2e;
   prm.status = g.status;

@@ -62,6 +62,7 @@ struct Params {
   float* lse;
   int64_t S, S_pad;
   int hq, hkv, G, n_qtiles, slots_per_kv;
+  int band;               // head slots per band of the CTA order (usp::cta_coords)
   int causal;             // 0: every key of the row's document is visible
   int64_t k_lo, k_hi;     // key window: only rows [k_lo, k_hi) are keys
   float scale_log2;
@@ -150,9 +151,10 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- tile coordinates (heaviest causal tiles first)
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;
-  const int y = blockIdx.y;
+  // ---- tile coordinates (rank 0 = the last, heaviest causal query tile)
+  int rank, y;
+  usp::cta_coords(p.n_qtiles, p.band, rank, y);
+  const int qt = p.n_qtiles - 1 - rank;
   const int per_g = p.hkv * p.slots_per_kv;
   const int g = y / per_g;
   const int jk = (y % per_g) / p.slots_per_kv;
@@ -437,8 +439,13 @@ cudaError_t launch_fwd(const usp::Geometry& g, const CUtensorMap& mq, const CUte
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, NH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)prm.n_qtiles, (unsigned)(g.P * g.hkv * prm.slots_per_kv));
-  attn_fwd_tc_kernel<D, NH><<<grid, 384, C::SMEM, st>>>(mq, mk, mv, prm);
+  const int n_y = g.P * g.hkv * prm.slots_per_kv;
+  const int64_t n_cta = (int64_t)prm.n_qtiles * n_y;
+  if (n_cta > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  Params pb = prm;
+  pb.band = usp::cta_band(prm.n_qtiles, n_y);
+  dim3 grid((unsigned)n_cta);
+  attn_fwd_tc_kernel<D, NH><<<grid, 384, C::SMEM, st>>>(mq, mk, mv, pb);
   usp_count_launches(1);
   return cudaGetLastError();
 }

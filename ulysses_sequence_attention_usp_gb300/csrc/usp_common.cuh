@@ -18,6 +18,41 @@ __device__ __forceinline__ void set_status(unsigned* word, unsigned bits) {
   if (word) atomicOr(word, bits);
 }
 
+// Order of the CTAs of an attention launch over n_tiles row tiles x n_y head
+// slots (a 1-D grid of n_tiles * n_y): bands of `band` consecutive head
+// slots run one after the other; inside a band the tile rank varies slowest.
+// Rank 0 is a kernel's heaviest causal tile, so the heaviest tiles of all the
+// band's heads start first, while the heads running at the same time stay
+// few enough to share their K/V (or Q/dO) tiles in L2.  Returns the tile
+// rank and the head slot of this CTA.
+__device__ __forceinline__ void cta_coords(int n_tiles, int band, int& rank, int& y) {
+  const unsigned n_y = gridDim.x / (unsigned)n_tiles;
+  const unsigned per_band = (unsigned)band * (unsigned)n_tiles;
+  const unsigned b = blockIdx.x / per_band;
+  const unsigned l = blockIdx.x - b * per_band;
+  const unsigned w = min((unsigned)band, n_y - b * (unsigned)band);
+  rank = (int)(l / w);
+  y = (int)(b * (unsigned)band + l % w);
+}
+
+// Band width for cta_coords: the smallest power of two (at most n_y) whose
+// band holds at least one CTA per SM, so that a band's heaviest tiles never
+// wait behind a whole band of other heads (the tail of a small problem),
+// while a large problem keeps one head per band.
+inline int cta_band(int n_tiles, int n_y) {
+  static int n_sm = 0;
+  if (n_sm == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n_sm <= 0)
+      n_sm = 1;
+  }
+  int band = 1;
+  while (band < n_y && (int64_t)band * n_tiles < n_sm) band *= 2;
+  return band < n_y ? band : (n_y > 0 ? n_y : 1);
+}
+
 // Host side helpers (usp_api.cu).
 struct Geometry {
   int64_t S, S_pad, S_loc;
