@@ -537,3 +537,81 @@ def ulysses(q, k, v, do, cu, cos, sin, scale, P, causal=True, zigzag=False):
     lse = lse_h.reshape(Hq, S_pad)[:, :S]
     return dict(o=o, lse=lse, loss=float((o * do).sum()),
                 dq=to_seq(dq_h)[:S], dk=to_seq(dk_h)[:S], dv=to_seq(dv_h)[:S])
+
+
+# ---------------------------------------------------------------------------
+# Context parallelism with a K/V all-gather (basetenlabs/Megatron-LM PR #7,
+# "GLM-5.2 131k context parallelism", Purpose: the CP forward all-gathers the
+# KV of every rank and its backward reduce-scatters dKV; contiguous
+# partition; positions from the global cu_seqlens).  Reading: P ranks hold
+# contiguous shards of S_loc padded rows of Q, K, V and dO with all heads, so
+# no head count has to be divisible by P.  Each rank rotates its own rows at
+# their global positions, gathers the K/V shards of all ranks in rank order
+# (which is the global row order), attends its query rows to every key with
+# the global causal / document mask, and in the backward computes dQ for its
+# rows and partial dK, dV over all key rows from its query rows alone.  The
+# partials of all ranks are summed and each rank keeps its own shard's rows
+# (the reduce-scatter), which it rotates back.
+# ---------------------------------------------------------------------------
+
+
+def allgather_cp(q, k, v, do, cu, cos, sin, scale, P, causal=True, return_partials=False):
+    """The K/V all-gather CP path over P virtual ranks (fp64 inputs [S][H][D]).
+    Returns the same dict as :func:`full_sequence`; with ``return_partials``
+    also each rank's pre-reduction dK/dV partials, [P][S_pad][Hkv][D] in the
+    rotated frame."""
+    S, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if Hkv < 1 or Hq % Hkv:
+        raise ValueError("Hq must be a multiple of Hkv")
+    G = Hq // Hkv
+    pos, doc = positions_docs(S, P, cu)
+    S_pad = pos.shape[0]
+    S_loc = S_pad // P
+    rows = [np.arange(r * S_loc, (r + 1) * S_loc) for r in range(P)]
+    padded = {n: shard_pad(x, P) for n, x in (("q", q), ("k", k), ("v", v), ("do", do))}
+    shard = {n: [x[rows[r]] for r in range(P)] for n, x in padded.items()}
+    # every rank rotates its own Q and K rows at their global positions
+    q_rot = [rope_rotate(shard["q"][r], pos[rows[r]], cos, sin) for r in range(P)]
+    k_rot = [rope_rotate(shard["k"][r], pos[rows[r]], cos, sin) for r in range(P)]
+    # all-gather: the K/V shards of all ranks, concatenated in rank order
+    k_all = np.concatenate(k_rot)
+    v_all = np.concatenate(shard["v"])
+    o_sh, lse_sh, dq_sh = [], [], []
+    dk_part = np.zeros((P, S_pad, Hkv, D))
+    dv_part = np.zeros((P, S_pad, Hkv, D))
+    for r in range(P):
+        # rank r's query rows sit at their global rows, so that the mask and
+        # the causal order use global indices
+        q_glob = np.zeros((S_pad, Hq, D))
+        do_glob = np.zeros((S_pad, Hq, D))
+        q_glob[rows[r]] = q_rot[r]
+        do_glob[rows[r]] = shard["do"][r]
+        o_r = np.zeros((S_loc, Hq, D))
+        lse_r = np.zeros((Hq, S_loc))
+        dq_r = np.zeros((S_loc, Hq, D))
+        for h in range(Hq):
+            kh, vh = k_all[:, h // G], v_all[:, h // G]
+            o_r[:, h], lse_r[h] = attention_rows(q_glob[:, h], kh, vh, doc, rows[r], scale,
+                                                 causal)
+            a, b, c = attention_bwd_head(q_glob[:, h], kh, vh, do_glob[:, h], doc, scale,
+                                         rows=rows[r], causal=causal)
+            dq_r[:, h] = a
+            dk_part[r, :, h // G] += b
+            dv_part[r, :, h // G] += c
+        o_sh.append(o_r)
+        lse_sh.append(lse_r)
+        dq_sh.append(rope_rotate(dq_r, pos[rows[r]], cos, sin, inverse=True))
+    # reduce-scatter: sum the partials of all ranks, rank r keeps its rows
+    dk_sum = dk_part.sum(axis=0)
+    dv_sum = dv_part.sum(axis=0)
+    dk_sh = [rope_rotate(dk_sum[rows[r]], pos[rows[r]], cos, sin, inverse=True)
+             for r in range(P)]
+    dv_sh = [dv_sum[rows[r]] for r in range(P)]
+    o = np.concatenate(o_sh)[:S]
+    out = dict(o=o, lse=np.concatenate(lse_sh, axis=1)[:, :S], loss=float((o * do).sum()),
+               dq=np.concatenate(dq_sh)[:S], dk=np.concatenate(dk_sh)[:S],
+               dv=np.concatenate(dv_sh)[:S])
+    if return_partials:
+        out["dk_part"], out["dv_part"] = dk_part, dv_part
+    return out
