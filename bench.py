@@ -258,7 +258,8 @@ def run_usp(args, wl, inp):
     from ulysses_sequence_attention_usp_gb300 import build as _build
     _build.build()
     from ulysses_sequence_attention_usp_gb300 import binding as B
-    from ulysses_sequence_attention_usp_gb300.pipeline import UlyssesAttention
+    from ulysses_sequence_attention_usp_gb300.pipeline import (AllGatherCPAttention,
+                                                               UlyssesAttention)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -272,44 +273,88 @@ def run_usp(args, wl, inp):
         return torch.from_numpy(bits.view(np.int16)).to(dev).view(torch.bfloat16)
 
     causal = not args.bidirectional
-    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
-                          rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
-                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
-                          causal=causal, zigzag=args.zigzag, ring=args.ring)
+    allgather = args.cp == "allgather"
+
+    def make_pipeline(rope_table=None):
+        if allgather:
+            return AllGatherCPAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                                        rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
+                                        yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len,
+                                        device=dev, rope_table=rope_table, causal=causal)
+        return UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                                rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
+                                yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
+                                rope_table=rope_table, causal=causal, zigzag=args.zigzag,
+                                ring=args.ring)
+
+    ua = make_pipeline()
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     st = torch.cuda.current_stream(dev)
     d = ua.dims
+    rows = getattr(ua, "S_pad", wl.S)          # rows of the sequence-layout buffers
+    bq = rows * wl.Hq * wl.D * 2
+    bkv = rows * wl.Hkv * wl.D * 2
+    tab = rows * wl.D * 4                      # one (cos, sin) row per position
 
-    # staged step with events between the calls (all on `st`)
-    stage_names = ["pad_qkv", "repack_qkv", "attn_fwd", "repack_o", "pad_do", "repack_do",
-                   "attn_bwd", "repack_grads"]
+    # the stages of one step, in order (all on `st`), and the algorithmic
+    # bytes of the permutation / RoPE stages
+    if allgather:
+        stages = [
+            ("positions", lambda: B.usp_pad_shard(d, None, 0, None, ua.pos, ua.doc, st)),
+            ("rope_qk", lambda: (
+                B.usp_seq_to_head_rope(d, q, wl.Hq, ua.pos, ua.rope, ua.rope_len, 1, ua.q_r, st),
+                B.usp_seq_to_head_rope(d, k, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1, ua.k_r,
+                                       st))),
+            ("attn_fwd", lambda: B.usp_attn_fwd(d, ua.q_r, ua.k_r, v, ua.doc, ua.o, ua.lse, st)),
+            ("attn_bwd", lambda: B.usp_attn_bwd(d, ua.q_r, ua.k_r, v, ua.o, ua.lse, do, ua.doc,
+                                                ua.dq_r, ua.dk_r, ua.dv, ua.ws, ua.ws_bytes,
+                                                st)),
+            ("rope_grads", lambda: (
+                B.usp_head_to_seq(d, ua.dq_r, wl.Hq, ua.pos, ua.rope, ua.rope_len, -1, ua.dq,
+                                  st),
+                B.usp_head_to_seq(d, ua.dk_r, wl.Hkv, ua.pos, ua.rope, ua.rope_len, -1, ua.dk,
+                                  st))),
+        ]
+        rep_bytes = {"rope_qk": 2 * (bq + bkv) + 2 * tab, "rope_grads": 2 * (bq + bkv) + 2 * tab}
+    else:
+        stages = [
+            ("pad_qkv", lambda: (
+                B.usp_pad_shard(d, q, wl.Hq, ua.q_seq, ua.pos, ua.doc, st),
+                B.usp_pad_shard(d, k, wl.Hkv, ua.k_seq, None, None, st),
+                B.usp_pad_shard(d, v, wl.Hkv, ua.v_seq, None, None, st))),
+            ("repack_qkv", lambda: (
+                B.usp_seq_to_head_rope(d, ua.q_seq, wl.Hq, ua.pos, ua.rope, ua.rope_len, 1,
+                                       ua.q_h, st),
+                B.usp_seq_to_head_rope(d, ua.k_seq, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1,
+                                       ua.k_h, st),
+                B.usp_seq_to_head_rope(d, ua.v_seq, wl.Hkv, None, None, 0, 0, ua.v_h, st))),
+            ("attn_fwd", lambda: ua.attention_forward(st)),     # one launch, or the ring steps
+            ("repack_o", lambda: B.usp_head_to_seq(d, ua.o_h, wl.Hq, None, None, 0, 0, ua.o, st)),
+            ("pad_do", lambda: B.usp_pad_shard(d, do, wl.Hq, ua.do_seq, None, None, st)),
+            ("repack_do", lambda: B.usp_seq_to_head_rope(d, ua.do_seq, wl.Hq, None, None, 0, 0,
+                                                         ua.do_h, st)),
+            ("attn_bwd", lambda: B.usp_attn_bwd(d, ua.q_h, ua.k_h, ua.v_h, ua.o_h, ua.lse,
+                                                ua.do_h, ua.doc, ua.dq_h, ua.dk_h, ua.dv_h,
+                                                ua.ws, ua.ws_bytes, st)),
+            ("repack_grads", lambda: (
+                B.usp_head_to_seq(d, ua.dq_h, wl.Hq, ua.pos, ua.rope, ua.rope_len, -1, ua.dq,
+                                  st),
+                B.usp_head_to_seq(d, ua.dk_h, wl.Hkv, ua.pos, ua.rope, ua.rope_len, -1, ua.dk,
+                                  st),
+                B.usp_head_to_seq(d, ua.dv_h, wl.Hkv, None, None, 0, 0, ua.dv, st))),
+        ]
+        rep_bytes = {"repack_qkv": 2 * (bq + 2 * bkv) + 2 * tab, "repack_o": 2 * bq,
+                     "repack_do": 2 * bq, "repack_grads": 2 * (bq + 2 * bkv) + 2 * tab}
+    stage_names = [n for n, _ in stages]
+    n_marks = len(stages) + 1
 
     def step(ev=None):
-        mark = (lambda i: ev[i].record(st)) if ev is not None else (lambda i: None)
-        mark(0)
-        B.usp_pad_shard(d, q, wl.Hq, ua.q_seq, ua.pos, ua.doc, st)
-        B.usp_pad_shard(d, k, wl.Hkv, ua.k_seq, None, None, st)
-        B.usp_pad_shard(d, v, wl.Hkv, ua.v_seq, None, None, st)
-        mark(1)
-        B.usp_seq_to_head_rope(d, ua.q_seq, wl.Hq, ua.pos, ua.rope, ua.rope_len, 1, ua.q_h, st)
-        B.usp_seq_to_head_rope(d, ua.k_seq, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1, ua.k_h, st)
-        B.usp_seq_to_head_rope(d, ua.v_seq, wl.Hkv, None, None, 0, 0, ua.v_h, st)
-        mark(2)
-        ua.attention_forward(st)           # one launch, or the ring steps
-        mark(3)
-        B.usp_head_to_seq(d, ua.o_h, wl.Hq, None, None, 0, 0, ua.o, st)
-        mark(4)
-        B.usp_pad_shard(d, do, wl.Hq, ua.do_seq, None, None, st)
-        mark(5)
-        B.usp_seq_to_head_rope(d, ua.do_seq, wl.Hq, None, None, 0, 0, ua.do_h, st)
-        mark(6)
-        B.usp_attn_bwd(d, ua.q_h, ua.k_h, ua.v_h, ua.o_h, ua.lse, ua.do_h, ua.doc, ua.dq_h,
-                       ua.dk_h, ua.dv_h, ua.ws, ua.ws_bytes, st)
-        mark(7)
-        B.usp_head_to_seq(d, ua.dq_h, wl.Hq, ua.pos, ua.rope, ua.rope_len, -1, ua.dq, st)
-        B.usp_head_to_seq(d, ua.dk_h, wl.Hkv, ua.pos, ua.rope, ua.rope_len, -1, ua.dk, st)
-        B.usp_head_to_seq(d, ua.dv_h, wl.Hkv, None, None, 0, 0, ua.dv, st)
-        mark(8)
+        for j, (_, call) in enumerate(stages):
+            if ev is not None:
+                ev[j].record(st)
+            call()
+        if ev is not None:
+            ev[len(stages)].record(st)
 
     for _ in range(args.warmup):
         step()
@@ -320,7 +365,8 @@ def run_usp(args, wl, inp):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_marks)]
+           for _ in range(args.steps)]
     clocks = ClockSampler(gpu_bus_id(torch))
     clocks.start()
     barrier()
@@ -345,19 +391,7 @@ def run_usp(args, wl, inp):
     # then HBM bandwidth.  Median of FLUSH_ITERS calls of each stage.
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 << 20)
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    rep_calls = {
-        "repack_qkv": lambda: (
-            B.usp_seq_to_head_rope(d, ua.q_seq, wl.Hq, ua.pos, ua.rope, ua.rope_len, 1, ua.q_h, st),
-            B.usp_seq_to_head_rope(d, ua.k_seq, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1, ua.k_h, st),
-            B.usp_seq_to_head_rope(d, ua.v_seq, wl.Hkv, None, None, 0, 0, ua.v_h, st)),
-        "repack_o": lambda: B.usp_head_to_seq(d, ua.o_h, wl.Hq, None, None, 0, 0, ua.o, st),
-        "repack_do": lambda: B.usp_seq_to_head_rope(d, ua.do_seq, wl.Hq, None, None, 0, 0,
-                                                    ua.do_h, st),
-        "repack_grads": lambda: (
-            B.usp_head_to_seq(d, ua.dq_h, wl.Hq, ua.pos, ua.rope, ua.rope_len, -1, ua.dq, st),
-            B.usp_head_to_seq(d, ua.dk_h, wl.Hkv, ua.pos, ua.rope, ua.rope_len, -1, ua.dk, st),
-            B.usp_head_to_seq(d, ua.dv_h, wl.Hkv, None, None, 0, 0, ua.dv, st)),
-    }
+    rep_calls = {n: c for n, c in stages if n in rep_bytes}
     flushed_ms = {}
     with torch.cuda.stream(st):
         for name, call in rep_calls.items():
@@ -382,11 +416,7 @@ def run_usp(args, wl, inp):
     # pipeline's reuse after its previous step's copies.
     pin = lambda a: torch.from_numpy(a.view(np.int16)).pin_memory()  # noqa: E731
     h_in = [pin(inp.q), pin(inp.k), pin(inp.v), pin(inp.do)]
-    ua2 = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
-                           rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
-                           yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len, device=dev,
-                           rope_table=ua.rope_host, causal=causal, zigzag=args.zigzag,
-                           ring=args.ring)
+    ua2 = make_pipeline(ua.rope_host)
     pipes = [(ua, (q, k, v, do)), (ua2, tuple(torch.empty_like(t) for t in (q, k, v, do)))]
     h_out = [[torch.empty(t.shape, dtype=torch.int16).pin_memory()
               for t in (ua.o, ua.dq, ua.dk, ua.dv)] for _ in range(2)]
@@ -456,11 +486,6 @@ def run_usp(args, wl, inp):
         value = aggregate_throughput(world, wl.S, args.steps, elapsed)
         t_fwd = stage_ms["attn_fwd"] / 1e3
         t_bwd = stage_ms["attn_bwd"] / 1e3
-        bq = ua.S_pad * wl.Hq * wl.D * 2
-        bkv = ua.S_pad * wl.Hkv * wl.D * 2
-        tab = ua.S_pad * wl.D * 4                  # one (cos, sin) row per position
-        rep_bytes = {"repack_qkv": 2 * (bq + 2 * bkv) + 2 * tab, "repack_o": 2 * bq,
-                     "repack_do": 2 * bq, "repack_grads": 2 * (bq + 2 * bkv) + 2 * tab}
         rep_t = sum(stage_ms[n] for n in rep_bytes) / 1e3
         rep_gbs_step = sum(rep_bytes.values()) / rep_t / 1e9
         rep_tf = sum(flushed_ms[n] for n in rep_bytes) / 1e3
@@ -477,16 +502,20 @@ def run_usp(args, wl, inp):
                        "D": wl.D, "rope": ("yarn x%g to %d" % (wl.yarn_factor, wl.rope_len)
                                            if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
                        "attention": "causal" if causal else "bidirectional",
-                       "shards": "zigzag" if args.zigzag else "contiguous",
+                       "shards": ("contiguous, K/V all-gather context parallelism"
+                                  if allgather else "zigzag" if args.zigzag else "contiguous"),
                        "ring": args.ring,
-                       "parallelism": f"replicas x{world} (P={wl.P} virtual shards per GPU)",
+                       "parallelism": (f"replicas x{world} (P={wl.P} virtual CP ranks per GPU)"
+                                       if allgather else
+                                       f"replicas x{world} (P={wl.P} virtual shards per GPU)"),
                        "l2": ("step: inputs larger than L2 (Q alone %.2f GB), no flush; "
                               "repack GB/s: each stage timed alone after a %d MB memset"
                               % (bq / 1e9, 2 * l2 >> 20))},
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
                          "bound": "tensor", "achieved": bwd_tf,
                          "peak": peak_t, "unit": "TFLOP/s", "frac": bwd_tf / peak_t,
-                         "traffic": measured_traffic(wl.name),
+                         "traffic": (measured_traffic(wl.name)
+                                     if causal and not allgather else None),
                          "peak_source": f"{src} (sustained bf16)",
                          "flops_per_launch": f_bwd},
             "attention": {"fwd_tflops": f_fwd / t_fwd / 1e12, "bwd_tflops": bwd_tf,
@@ -496,7 +525,8 @@ def run_usp(args, wl, inp):
                           "bwd_flops": {"convention_2.5x": f_bwd, "strict_no_recompute": f_bwd_strict},
                           "fwd_ms": t_fwd * 1e3, "bwd_ms": t_bwd * 1e3,
                           "attended_pairs": pairs},
-            "repack": {"gbps": rep_gbs, "frac": rep_gbs / peaks["hbm_gbs"],
+            "repack": {"stages": list(rep_bytes), "gbps": rep_gbs,
+                       "frac": rep_gbs / peaks["hbm_gbs"],
                        "peak_gbps": peaks["hbm_gbs"], "peak_source": src,
                        "bytes_per_step": sum(rep_bytes.values()),
                        "timing": "each stage alone, L2 flushed before each call, "
@@ -541,7 +571,12 @@ def main():
                     help="zigzag shard layout (rank r holds chunks r and 2P-1-r of 2P)")
     ap.add_argument("--ring", type=int, default=1,
                     help="ring steps of the forward (key windows merged by log-sum-exp)")
+    ap.add_argument("--cp", choices=["ulysses", "allgather"], default="ulysses",
+                    help="sequence parallelism: Ulysses all-to-all (default) or context "
+                         "parallelism with a K/V all-gather")
     args = ap.parse_args()
+    if args.cp == "allgather" and (args.zigzag or args.ring != 1):
+        ap.error("--cp allgather runs contiguous shards without ring steps")
     from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, make_inputs
     wl = WORKLOADS[args.workload]
     if args.impl == "reference" and int(os.environ.get("RANK", "0")) != 0:

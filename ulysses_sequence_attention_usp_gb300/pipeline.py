@@ -129,3 +129,105 @@ class UlyssesAttention:
 
     def check(self, stream=None):
         B.usp_device_status(stream)
+
+
+class AllGatherCPAttention:
+    """Context parallelism with a K/V all-gather over P virtual ranks
+    (basetenlabs/Megatron-LM PR #7 "GLM-5.2 131k context parallelism",
+    Purpose: the CP forward all-gathers the KV of every rank, the backward
+    reduce-scatters dKV; contiguous partition; positions from the global
+    cu_seqlens).
+
+    Rank r holds the contiguous rows [r*S_loc, (r+1)*S_loc) of Q, K, V with
+    all heads, so no head count has to be divisible by P: this is the
+    layout for fewer KV heads than ranks, which the all-to-all cannot shard.
+    On one GPU the shards are row ranges of one sequence-layout buffer, so
+    the all-gather of K/V is that buffer itself and the reduce-scatter of
+    dK/dV is the key-stationary backward pass's sum over the query rows of
+    every rank.  A step is therefore
+
+      positions/documents -> RoPE of Q and K at global positions
+      -> attention of every rank's rows over all keys (one launch)
+      -> backward (delta, dK/dV, dQ) -> inverse RoPE of dQ and dK
+
+    with the library's entry points called on a one-shard geometry; V, O,
+    dO and dV are used in place, never copied.  Rows are not padded: equal
+    shards on P devices would add only masked rows (document -1), which
+    change no valid output.
+    """
+
+    def __init__(self, S, P, Hq, Hkv, D, cu_seqlens=None, rope_base=1.0e4, yarn_factor=1.0,
+                 yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None,
+                 causal=True):
+        self.S, self.P, self.Hq, self.Hkv, self.D = int(S), int(P), int(Hq), int(Hkv), int(D)
+        if self.P < 1:
+            raise ValueError("P must be >= 1")
+        self.S_loc = -(-self.S // self.P)
+        self.device = torch.device(device)
+        dev = self.device
+        self.cu_host = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, np.int32)
+        self.cu_dev = None if self.cu_host is None else torch.from_numpy(self.cu_host).to(dev)
+        self.causal = bool(causal)
+        # one shard holding every row: the gathered view all ranks share
+        self.dims = B.make_dims(S, 1, Hq, Hkv, D, self.cu_dev, self.cu_host, scale, causal)
+        self.rope_len = int(rope_len) if rope_len else self.S
+        if rope_table is None:
+            rope_table = B.usp_rope_table(self.rope_len, D, rope_base, yarn_factor, yarn_orig_ctx)
+        self.rope_host = rope_table
+        self.rope = torch.from_numpy(np.ascontiguousarray(rope_table)).to(dev)
+        S_ = self.S
+        bf = torch.bfloat16
+        e = lambda *s, dt=bf: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+        self.pos = e(S_, dt=torch.int32)
+        self.doc = e(S_, dt=torch.int32)
+        self.q_r, self.k_r = e(S_, Hq, D), e(S_, Hkv, D)        # rotated Q, K
+        self.o = e(S_, Hq, D)
+        self.lse = e(Hq, S_, dt=torch.float32)
+        self.dq_r, self.dk_r = e(S_, Hq, D), e(S_, Hkv, D)      # gradients, rotated frame
+        self.dq, self.dk, self.dv = e(S_, Hq, D), e(S_, Hkv, D), e(S_, Hkv, D)
+        self.ws_bytes = B.usp_attn_bwd_workspace(self.dims)
+        self.ws = e(max(1, self.ws_bytes), dt=torch.uint8)
+        self._v = None
+
+    def shard(self, x, r):
+        """Rank r's rows of a sequence-layout tensor (a view)."""
+        return x[r * self.S_loc:min(self.S, (r + 1) * self.S_loc)]
+
+    def forward(self, q, k, v, stream=None):
+        """q [S][Hq][D], k/v [S][Hkv][D] bf16 contiguous device tensors
+        (pre-RoPE, every rank's rows in rank order).  Returns O [S][Hq][D]."""
+        d, st = self.dims, stream
+        for t in (q, k, v):
+            if not t.is_contiguous():
+                raise ValueError("q, k, v must be contiguous")
+        B.usp_pad_shard(d, None, 0, None, self.pos, self.doc, st)
+        B.usp_seq_to_head_rope(d, q, self.Hq, self.pos, self.rope, self.rope_len, 1, self.q_r,
+                               st)
+        B.usp_seq_to_head_rope(d, k, self.Hkv, self.pos, self.rope, self.rope_len, 1, self.k_r,
+                               st)
+        self._v = v
+        B.usp_attn_fwd(d, self.q_r, self.k_r, v, self.doc, self.o, self.lse, st)
+        return self.o
+
+    def backward(self, do, stream=None):
+        """do [S][Hq][D] bf16 contiguous.  Returns dQ, dK, dV [S][H][D], the
+        gradients of the pre-RoPE inputs (rank r's rows are its shard)."""
+        if self._v is None:
+            raise RuntimeError("backward before forward")
+        if not do.is_contiguous():
+            raise ValueError("do must be contiguous")
+        d, st = self.dims, stream
+        B.usp_attn_bwd(d, self.q_r, self.k_r, self._v, self.o, self.lse, do, self.doc,
+                       self.dq_r, self.dk_r, self.dv, self.ws, self.ws_bytes, st)
+        B.usp_head_to_seq(d, self.dq_r, self.Hq, self.pos, self.rope, self.rope_len, -1,
+                          self.dq, st)
+        B.usp_head_to_seq(d, self.dk_r, self.Hkv, self.pos, self.rope, self.rope_len, -1,
+                          self.dk, st)
+        return self.dq, self.dk, self.dv
+
+    def step(self, q, k, v, do, stream=None):
+        self.forward(q, k, v, stream)
+        return self.backward(do, stream)
+
+    def check(self, stream=None):
+        B.usp_device_status(stream)
