@@ -69,7 +69,15 @@ typedef enum {
 /* Problem description shared by all calls. */
 typedef struct {
   int64_t S;                        /* valid tokens (sum of document lengths), >= 0 */
-  int32_t P;                        /* Ulysses degree = number of virtual shards, >= 1 */
+  int32_t P;                        /* Ulysses degree = number of virtual shards, >= 1.
+                                       P = 1 is one shard holding every row: its
+                                       head layout is the sequence layout, so
+                                       the calls then rotate in place of the
+                                       all-to-all and attend over [S][H][D]
+                                       buffers directly -- the data path of
+                                       context parallelism with a K/V
+                                       all-gather (Megatron-LM #7, Purpose),
+                                       which takes any Hkv dividing Hq */
   int32_t Hq, Hkv, D;               /* query heads, key/value heads, head dim (64|128) */
   const int32_t* cu_seqlens;        /* device int32 [n_docs+1], global document
                                        boundaries; NULL => one document [0,S) */

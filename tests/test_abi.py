@@ -137,6 +137,17 @@ def test_empty_sequence_is_a_no_op():
     assert B.raw_call("usp_pad_shard", ctypes.byref(d), FAKE, 4, FAKE, FAKE, FAKE, None) == 0
 
 
+def test_one_shard_geometry_takes_fewer_kv_heads_than_ranks():
+    # the K/V all-gather CP path runs on P = 1, which accepts any Hkv | Hq;
+    # the same heads over P = 4 shards are refused by the all-to-all
+    assert _fwd(_dims(S=0, P=1, Hq=4, Hkv=1)) == 0
+    assert _fwd(_dims(S=0, P=4, Hq=4, Hkv=1)) == 2
+    d = _dims(S=0, P=1, Hq=4, Hkv=1)
+    for H in (4, 1):
+        assert B.raw_call("usp_seq_to_head_rope", ctypes.byref(d), FAKE, H, FAKE, FAKE,
+                          ctypes.c_int64(0), 0, FAKE + 4096, None) == 0
+
+
 @pytest.mark.parametrize("n,D,base,f,L", [(300, 64, 1.0e4, 1.0, 0), (4096, 128, 1.0e6, 1.0, 0),
                                           (131072, 128, 1.0e6, 4.0, 32768)])
 def test_library_rope_table_matches_oracle(n, D, base, f, L):
