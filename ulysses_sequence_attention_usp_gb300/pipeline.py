@@ -63,6 +63,7 @@ class UlyssesAttention:
             self.o_part = e(P, Sp, hq, D)
             self.lse_part = e(P, hq, Sp, dt=torch.float32)
             self.o_acc = e(P, Sp, hq, D, dt=torch.float32)
+        self._forward_done = False
 
     # -- steps -------------------------------------------------------------
     def forward(self, q, k, v, stream=None):
@@ -80,6 +81,7 @@ class UlyssesAttention:
         B.usp_seq_to_head_rope(d, self.v_seq, self.Hkv, None, None, 0, 0, self.v_h, st)
         self.attention_forward(st)
         B.usp_head_to_seq(d, self.o_h, self.Hq, None, None, 0, 0, self.o, st)
+        self._forward_done = True
         return self.o
 
     def attention_forward(self, stream=None):
@@ -106,6 +108,8 @@ class UlyssesAttention:
         """do [S][Hq][D] bf16 (dL/dO).  Returns dQ, dK, dV [S_pad][H][D]: the
         gradients of the pre-RoPE sequence-sharded inputs, in the same shard
         layout as O."""
+        if not self._forward_done:
+            raise RuntimeError("backward before forward")
         d, st = self.dims, stream
         B.usp_pad_shard(d, do, self.Hq, self.do_seq, None, None, st)
         B.usp_seq_to_head_rope(d, self.do_seq, self.Hq, None, None, 0, 0, self.do_h, st)
