@@ -219,6 +219,21 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def workload_config(args, wl, world=1):
+    """The `config` keys both arms print for the same flags."""
+    allgather = args.cp == "allgather"
+    return {"workload": wl.name, "S": wl.S, "P": wl.P, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+            "rope": ("yarn x%g to %d" % (wl.yarn_factor, wl.rope_len)
+                     if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
+            "attention": "bidirectional" if args.bidirectional else "causal",
+            "shards": ("contiguous, K/V all-gather context parallelism"
+                       if allgather else "zigzag" if args.zigzag else "contiguous"),
+            "ring": args.ring,
+            "parallelism": (f"replicas x{world} (P={wl.P} virtual CP ranks per GPU)"
+                            if allgather else
+                            f"replicas x{world} (P={wl.P} virtual shards per GPU)")}
+
+
 def run_reference(args, wl, inp):
     """--impl reference: the oracle, timed on host cores (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
@@ -240,8 +255,7 @@ def run_reference(args, wl, inp):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": full_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "S": wl.S, "P": wl.P, "Hq": wl.Hq, "Hkv": wl.Hkv,
-                   "D": wl.D, "attention": "causal" if causal else "bidirectional"},
+        "config": workload_config(args, wl, args.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -498,19 +512,10 @@ def run_usp(args, wl, inp):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": wl.name, "S": wl.S, "P": wl.P, "Hq": wl.Hq, "Hkv": wl.Hkv,
-                       "D": wl.D, "rope": ("yarn x%g to %d" % (wl.yarn_factor, wl.rope_len)
-                                           if wl.yarn_factor > 1 else "base %g" % wl.rope_base),
-                       "attention": "causal" if causal else "bidirectional",
-                       "shards": ("contiguous, K/V all-gather context parallelism"
-                                  if allgather else "zigzag" if args.zigzag else "contiguous"),
-                       "ring": args.ring,
-                       "parallelism": (f"replicas x{world} (P={wl.P} virtual CP ranks per GPU)"
-                                       if allgather else
-                                       f"replicas x{world} (P={wl.P} virtual shards per GPU)"),
-                       "l2": ("step: inputs larger than L2 (Q alone %.2f GB), no flush; "
-                              "repack GB/s: each stage timed alone after a %d MB memset"
-                              % (bq / 1e9, 2 * l2 >> 20))},
+            "config": dict(workload_config(args, wl, world),
+                           l2=("step: inputs larger than L2 (Q alone %.2f GB), no flush; "
+                               "repack GB/s: each stage timed alone after a %d MB memset"
+                               % (bq / 1e9, 2 * l2 >> 20))),
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
                          "bound": "tensor", "achieved": bwd_tf,
                          "peak": peak_t, "unit": "TFLOP/s", "frac": bwd_tf / peak_t,
