@@ -219,6 +219,18 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def l2_note(step_in_bytes, l2_bytes):
+    """How L2 is treated by the timing, for the bench line's config."""
+    if step_in_bytes > l2_bytes:
+        step = ("step: inputs larger than L2 (%.2f GB of Q, K, V, dO), no flush"
+                % (step_in_bytes / 1e9))
+    else:
+        step = ("step: inputs smaller than L2 (%.1f MB of Q, K, V, dO), not flushed "
+                "between steps" % (step_in_bytes / 1e6))
+    return step + ("; repack GB/s: each stage timed alone after a %d MB memset"
+                   % (2 * l2_bytes >> 20))
+
+
 def workload_config(args, wl, world=1):
     """The `config` keys both arms print for the same flags."""
     allgather = args.cp == "allgather"
@@ -513,9 +525,7 @@ def run_usp(args, wl, inp):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
             "config": dict(workload_config(args, wl, world),
-                           l2=("step: inputs larger than L2 (Q alone %.2f GB), no flush; "
-                               "repack GB/s: each stage timed alone after a %d MB memset"
-                               % (bq / 1e9, 2 * l2 >> 20))),
+                           l2=l2_note(2 * (bq + bkv), l2)),
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
                          "bound": "tensor", "achieved": bwd_tf,
                          "peak": peak_t, "unit": "TFLOP/s", "frac": bwd_tf / peak_t,

@@ -39,3 +39,24 @@ def test_attended_pairs_match_the_mask(S, lens, causal):
     _, doc = O.positions_docs(S, 1, cu)
     vis = O._visible(np.arange(S), doc, causal)
     assert bench.attended_pairs(S, cu, causal) == int(vis.sum())
+
+
+def test_l2_note_says_whether_steps_are_l2_warm():
+    l2 = 129 << 20
+    big = bench.l2_note(2 * (983_040_000 + 245_760_000), l2)   # the 120K workload
+    small = bench.l2_note(2 * (256 * 4 * 64 * 2 + 256 * 2 * 64 * 2), l2)
+    assert "larger than L2" in big and "no flush" in big
+    assert "smaller than L2" in small and "not flushed" in small
+    assert "258 MB memset" in big and "258 MB memset" in small
+
+
+def test_both_arms_print_the_same_config_keys():
+    import types
+    wl = WORKLOADS["sp8_120k"]
+    for cp, zz, ring in (("ulysses", False, 1), ("ulysses", True, 1), ("ulysses", False, 4),
+                         ("allgather", False, 1)):
+        a = types.SimpleNamespace(cp=cp, bidirectional=False, zigzag=zz, ring=ring)
+        c = bench.workload_config(a, wl, 1)
+        assert c["workload"] == "sp8_120k" and c["S"] == 120000 and c["ring"] == ring
+        assert ("all-gather" in c["shards"]) == (cp == "allgather")
+        assert ("zigzag" in c["shards"]) == zz
