@@ -34,6 +34,9 @@
  * Conventions for every call:
  *   - Pointers are DEVICE pointers unless the name ends in _host.  The
  *     caller owns every buffer; no call allocates or frees device memory.
+ *     Buffer sizes are not passed and cannot be checked: each buffer must
+ *     hold the layout its argument documents for the given usp_dims (the
+ *     Python pipeline objects check tensor shapes before calling).
  *   - Tensor buffers must be 16-byte aligned; D must be 64 or 128.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream) and return after enqueueing.  Arguments are validated

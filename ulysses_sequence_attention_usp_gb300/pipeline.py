@@ -21,6 +21,22 @@ import torch
 from . import binding as B
 
 
+def _check_input(name, t, rows, heads, D, device):
+    """The C ABI cannot see buffer sizes, so a tensor of the wrong shape would
+    be read out of bounds on the device: check it here."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.device.type != device.type or (device.index is not None and
+                                        t.device.index != device.index):
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != (rows, heads, D):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {(rows, heads, D)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
 class UlyssesAttention:
     def __init__(self, S, P, Hq, Hkv, D, cu_seqlens=None, rope_base=1.0e4, yarn_factor=1.0,
                  yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None,
@@ -70,6 +86,8 @@ class UlyssesAttention:
         """q [S][Hq][D], k/v [S][Hkv][D] bf16 device tensors (pre-RoPE).
         Returns O [S_pad][Hq][D] in the sequence-sharded layout (global row
         order, or zigzag shard order when zigzag=True); padding rows are 0."""
+        for n, t, h in (("q", q, self.Hq), ("k", k, self.Hkv), ("v", v, self.Hkv)):
+            _check_input(n, t, self.S, h, self.D, self.device)
         d, st = self.dims, stream
         B.usp_pad_shard(d, q, self.Hq, self.q_seq, self.pos, self.doc, st)
         B.usp_pad_shard(d, k, self.Hkv, self.k_seq, None, None, st)
@@ -110,6 +128,7 @@ class UlyssesAttention:
         layout as O."""
         if not self._forward_done:
             raise RuntimeError("backward before forward")
+        _check_input("do", do, self.S, self.Hq, self.D, self.device)
         d, st = self.dims, stream
         B.usp_pad_shard(d, do, self.Hq, self.do_seq, None, None, st)
         B.usp_seq_to_head_rope(d, self.do_seq, self.Hq, None, None, 0, 0, self.do_h, st)
@@ -200,10 +219,9 @@ class AllGatherCPAttention:
     def forward(self, q, k, v, stream=None):
         """q [S][Hq][D], k/v [S][Hkv][D] bf16 contiguous device tensors
         (pre-RoPE, every rank's rows in rank order).  Returns O [S][Hq][D]."""
+        for n, t, h in (("q", q, self.Hq), ("k", k, self.Hkv), ("v", v, self.Hkv)):
+            _check_input(n, t, self.S, h, self.D, self.device)
         d, st = self.dims, stream
-        for t in (q, k, v):
-            if not t.is_contiguous():
-                raise ValueError("q, k, v must be contiguous")
         B.usp_pad_shard(d, None, 0, None, self.pos, self.doc, st)
         B.usp_seq_to_head_rope(d, q, self.Hq, self.pos, self.rope, self.rope_len, 1, self.q_r,
                                st)
@@ -218,8 +236,7 @@ class AllGatherCPAttention:
         gradients of the pre-RoPE inputs (rank r's rows are its shard)."""
         if self._v is None:
             raise RuntimeError("backward before forward")
-        if not do.is_contiguous():
-            raise ValueError("do must be contiguous")
+        _check_input("do", do, self.S, self.Hq, self.D, self.device)
         d, st = self.dims, stream
         B.usp_attn_bwd(d, self.q_r, self.k_r, self._v, self.o, self.lse, do, self.doc,
                        self.dq_r, self.dk_r, self.dv, self.ws, self.ws_bytes, st)
