@@ -457,6 +457,43 @@ def attention_bwd_head(q, k, v, do, doc, scale, rows=None, causal=True):
     return dq, dk, dv
 
 
+def attention_bwd_keys(q, k, v, do, doc, scale, keys, rows=None, causal=True):
+    """dK and dV of one head (fp64, q/k/v/do [T][D]) at the key rows ``keys``
+    only, summed over the query rows ``rows`` (default: all rows).
+
+    The same gradient as :func:`attention_bwd_head`, evaluated without the
+    full T x T matrices: each query row t first gets its own softmax
+    denominator LSE_t and output O_t from :func:`attention_rows` (over every
+    key it sees), and delta_t = dO_t . O_t, which equals sum_u P_tu dP_tu
+    because O_t = sum_u P_tu v_u.  Then, for the chosen keys only,
+    P_tu = exp(scale q_t.k_u - LSE_t), dP_tu = dO_t.v_u,
+    dS_tu = P_tu (dP_tu - delta_t), dK_u = scale sum_t dS_tu q_t and
+    dV_u = sum_t P_tu dO_t.  Row sets may be split into chunks and the
+    partial sums added (each row's terms depend on that row alone), which is
+    how long sequences are evaluated in parallel."""
+    T, D = q.shape
+    keys = np.asarray(keys, np.int64)
+    rows_all = np.arange(T) if rows is None else np.asarray(rows, np.int64)
+    dk = np.zeros((keys.shape[0], D))
+    dv = np.zeros((keys.shape[0], D))
+    for a in range(0, rows_all.shape[0], _ROW_CHUNK):
+        rows = rows_all[a:a + _ROW_CHUNK]
+        # causal: no key after the chunk's last row is visible to it
+        hi = int(rows.max()) + 1 if causal else T
+        o, lse = attention_rows(q[:hi], k[:hi], v[:hi], doc[:hi], rows, scale, causal)
+        delta = (do[rows] * o).sum(axis=1)
+        vis = _visible(rows, doc, causal)[:, keys]
+        has = np.isfinite(lse)
+        s = (q[rows] @ k[keys].T) * scale
+        p = np.where(vis & has[:, None],
+                     np.exp(s - np.where(has, lse, 0.0)[:, None]), 0.0)
+        dp = do[rows] @ v[keys].T
+        ds = p * (dp - delta[:, None])
+        dk += scale * (ds.T @ q[rows])
+        dv += p.T @ do[rows]
+    return dk, dv
+
+
 def attention_bwd(q, k, v, do, doc, scale, causal=True):
     """All heads: q/do[T][Hq][D], k/v[T][Hkv][D] -> dq, dk, dv (fp64).  dK and
     dV of a KV head are summed over the Hq/Hkv query heads that read it."""

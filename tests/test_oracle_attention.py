@@ -191,3 +191,62 @@ def test_padding_has_no_effect_on_valid_rows():
     r2 = O.ulysses(q, k, v, do, None, cos, sin, 0.3, 2)
     for key in ("o", "lse", "dq", "dk", "dv"):
         assert np.array_equal(r4[key], r2[key]) or np.allclose(r4[key], r2[key], atol=1e-13, rtol=0), key
+
+
+def _torch_grads_masked(q, k, v, do, doc, causal):
+    # one head, explicit boolean mask (same document, and u <= t if causal)
+    tq, tk, tv = (torch.from_numpy(x).clone().requires_grad_(True) for x in (q, k, v))
+    T = q.shape[0]
+    d = torch.from_numpy(doc)
+    mask = (d[:, None] == d[None, :]) & (d[:, None] >= 0)
+    if causal:
+        mask &= torch.ones(T, T, dtype=torch.bool).tril()
+    o = F.scaled_dot_product_attention(tq[None, None], tk[None, None], tv[None, None],
+                                       attn_mask=mask[None, None])[0, 0]
+    o = torch.where(mask.any(1, keepdim=True), o, torch.zeros_like(o))
+    (o * torch.from_numpy(do)).sum().backward()
+    return tk.grad.numpy(), tv.grad.numpy()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_bwd_keys_matches_torch_autograd_and_splits_over_row_chunks(causal):
+    # dK/dV at a few key rows, summed over all query rows, equal autograd's
+    # (documents of lengths 9, 1, 14 and 2 pad rows); the sum over disjoint
+    # row chunks equals the sum over all rows.
+    lens = [9, 1, 14]
+    T, D = sum(lens) + 2, 8
+    q, k, v, do = (_rand((T, D), s) for s in (31, 32, 33, 34))
+    _, doc = O.positions_docs(sum(lens), 1, np.concatenate([[0], np.cumsum(lens)]), S_pad=T)
+    keys = np.array([0, 3, 9, 10, 11, 23, 24])
+    dk, dv = O.attention_bwd_keys(q, k, v, do, doc, 1 / math.sqrt(D), keys, causal=causal)
+    tk, tv = _torch_grads_masked(q, k, v, do, doc, causal)
+    assert np.allclose(dk, tk[keys], atol=1e-12, rtol=0)
+    assert np.allclose(dv, tv[keys], atol=1e-12, rtol=0)
+    assert not dk[-1].any() and not dv[-1].any()          # a pad row is never a key
+    parts = [O.attention_bwd_keys(q, k, v, do, doc, 1 / math.sqrt(D), keys, rows=r,
+                                  causal=causal) for r in (np.arange(0, 7), np.arange(7, T))]
+    assert np.allclose(parts[0][0] + parts[1][0], dk, atol=1e-13, rtol=0)
+    assert np.allclose(parts[0][1] + parts[1][1], dv, atol=1e-13, rtol=0)
+
+
+def test_parallel_key_gradients_equal_the_direct_oracle():
+    # tests/oracle_pool.py (spawned workers over row chunks, used by the
+    # full-size GPU checks) against the whole-sequence oracle: pre-RoPE dK/dV
+    # of a GQA group's KV head at its first keys.
+    from oracle_pool import dkdv_keys
+    from ulysses_sequence_attention_usp_gb300.inputs import normal_bf16
+    T, G, D = 300, 3, 16
+    cu = np.array([0, 120, 300])
+    pos, doc = O.positions_docs(T, 1, cu)
+    cos, sin = O.rope_cos_sin(T, D, 1.0e4)
+    qb = normal_bf16((T, G, D), 7, "q")
+    kb, vb = normal_bf16((T, 1, D), 7, "k"), normal_bf16((T, 1, D), 7, "v")
+    dob = normal_bf16((T, G, D), 7, "do")
+    scale = 1 / math.sqrt(D)
+    f = O.bf16_to_f64
+    ref = O.full_sequence(f(qb), f(kb), f(vb), f(dob), cu, cos, sin, scale)
+    keys = np.arange(120, 130)          # first keys of the second document
+    dk, dv = dkdv_keys(qb, kb[:, 0], vb[:, 0], dob, pos, doc, cos, sin, scale, keys,
+                       np.arange(120, 300), chunk=64, workers=2)
+    assert np.allclose(dk, ref["dk"][keys, 0], atol=1e-12, rtol=0)
+    assert np.allclose(dv, ref["dv"][keys, 0], atol=1e-12, rtol=0)

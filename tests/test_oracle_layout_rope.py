@@ -167,6 +167,33 @@ def test_yarn_regimes_and_mscale():
     assert np.all(t[0, :, 0] == np.float32(1.1386294361119891))
 
 
+def test_yarn_ramp_hand_worked_golden():
+    # Correction range and interior ramp values worked out by hand from
+    # Peng et al. 2023, sec. 3.2, for the 131,072-token YaRN table of
+    # SpecForge PR #728, Accuracy Test (tests/golden/yarn_ramp.json holds the
+    # derivation).  An off-by-one in the floor/ceil of the correction range,
+    # a wrong ramp denominator or a ramp over the wrong index all move these.
+    g = _gold("yarn_ramp.json")
+    D, base, L, s = g["D"], g["base"], g["orig_ctx"], g["scale"]
+    two_ln_b = 2 * math.log(base)
+    assert D * math.log(L / (2 * math.pi * g["beta_fast"])) / two_ln_b == pytest.approx(
+        g["corr_dim_fast"], abs=1e-3)
+    assert D * math.log(L / (2 * math.pi * g["beta_slow"])) / two_ln_b == pytest.approx(
+        g["corr_dim_slow"], abs=1e-3)
+    yarn = O.rope_inv_freq(D, base, s, L)
+    for i, ratio in g["ratio_to_plain"].items():
+        plain = 10.0 ** (-6.0 * 2 * int(i) / D)
+        assert yarn[int(i)] == pytest.approx(plain * ratio, rel=1e-13), i
+    for i, e in g["inv_freq_exponent_of_10"].items():
+        ratio = g["ratio_to_plain"][i]
+        assert yarn[int(i)] == pytest.approx(10.0 ** e * ratio, rel=1e-13), i
+    # the ramp is linear in i between the two ends: equal steps of f_i * 0.75/17
+    lo, hi = g["ramp_lo"], g["ramp_hi"]
+    plain = O.rope_inv_freq(D, base)
+    steps = np.diff(yarn[lo:hi + 1] / plain[lo:hi + 1])
+    assert np.allclose(steps, -0.75 / (hi - lo), rtol=0, atol=1e-14)
+
+
 # ---------------------------------------------------------- bf16 RoPE recipe
 
 def _f32(v):
