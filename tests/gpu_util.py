@@ -83,6 +83,43 @@ class SampledOracle:
                                             wl.yarn_factor, wl.yarn_orig_ctx)
         self.q, self.k, self.v, self.do = q, k, v, do
         self._kr = {}
+        self._kb = {}
+        self._table = None
+
+    def table(self):
+        """The fp32 (cos, sin) table the GPU run is given (built by the oracle)."""
+        if self._table is None:
+            wl = self.wl
+            self._table = O.rope_table_f32(max(wl.table_len, self.S), wl.D, wl.rope_base,
+                                           wl.yarn_factor, wl.yarn_orig_ctx)
+        return self._table
+
+    def lse_rows_recipe(self, h, rows):
+        """LSE of head h at the given rows when the attention is fed the bf16
+        rotated Q and K of the fp32 recipe (the GPU's actual inputs): exact
+        fp64 attention of those bf16 values, so only the kernel's own
+        arithmetic separates the two."""
+        kh = h // self.G
+        if kh not in self._kb:
+            kr = O.rope_recipe_bf16(self.k[:, kh:kh + 1], self.pos[:self.S], self.table())
+            self._kb[kh] = O.bf16_to_f64(kr[:, 0])
+        rows = np.asarray(rows)
+        qr = np.zeros((self.S, self.wl.D))
+        qr[rows] = O.bf16_to_f64(O.rope_recipe_bf16(self.q[rows, h:h + 1], self.pos[rows],
+                                                    self.table())[:, 0])
+        _, lse = O.attention_rows(qr, self._kb[kh], O.bf16_to_f64(self.v[:, kh]), self.doc,
+                                  rows, self.scale, self.causal)
+        return lse
+
+    def dkv_keys(self, kh, keys, rows, workers=None):
+        """Pre-RoPE dK and dV of KV head kh at ``keys`` from every query row in
+        ``rows`` (all the rows that see them), evaluated over row chunks in
+        spawned worker processes (tests/oracle_pool.py)."""
+        from oracle_pool import dkdv_keys
+        G = self.G
+        return dkdv_keys(self.q[:, kh * G:(kh + 1) * G], self.k[:, kh], self.v[:, kh],
+                         self.do[:, kh * G:(kh + 1) * G], self.pos, self.doc, self.cos,
+                         self.sin, self.scale, keys, rows, causal=self.causal, workers=workers)
 
     def _rot(self, bits_rows, rows):
         x = O.bf16_to_f64(bits_rows)

@@ -57,16 +57,21 @@ def test_allgather_step_vs_oracle(case, causal):
         assert ag.shard(ag.o, r).shape[0] == max(0, min(wl.S, (r + 1) * S_loc) - r * S_loc)
 
 
-def test_allgather_full_workload_sampled():
+def _allgather_120k():
     wl = WORKLOADS["sp8_120k"]
     inp = make_inputs(wl, 0)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
     ag = AllGatherCPAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, rope_base=wl.rope_base,
                               yarn_factor=wl.yarn_factor, yarn_orig_ctx=wl.yarn_orig_ctx,
-                              rope_len=wl.rope_len)
+                              rope_len=wl.rope_len, rope_table=orc.table())
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     ag.step(q, k, v, do)
     ag.check()
-    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
+    return wl, inp, ag, orc
+
+
+def test_allgather_full_workload_sampled():
+    wl, inp, ag, orc = _allgather_120k()
     rng = np.random.default_rng(7)
     S = wl.S
     S_loc = -(-S // wl.P)
@@ -77,8 +82,22 @@ def test_allgather_full_workload_sampled():
         r_o, _ = orc.fwd_rows(h, rows)
         check_o(to_f64(ag.o[rows, h]), r_o)
         check_grad(to_f64(ag.dq[rows, h]), orc.dq_rows(h, rows), "dq")
+        check_lse(ag.lse[h, rows].cpu().numpy().astype(np.float64),
+                  orc.lse_rows_recipe(h, rows))
     lo = S - 48
     for kh in sorted({0, wl.Hkv - 1}):
         r_dk, r_dv = orc.dkv_tail(kh, lo, S)
         check_grad(to_f64(ag.dk[lo:S, kh]), r_dk, "dk")
         check_grad(to_f64(ag.dv[lo:S, kh]), r_dv, "dv")
+
+
+@pytest.mark.slow
+def test_allgather_120k_first_keys():
+    """dK/dV of keys 0..47, which all 120 000 query rows see (the longest
+    key-stationary loop; the sum over every rank's query rows is what the
+    reduce-scatter of dK/dV adds up)."""
+    wl, inp, ag, orc = _allgather_120k()
+    keys = np.arange(48)
+    r_dk, r_dv = orc.dkv_keys(0, keys, np.arange(wl.S))
+    check_grad(to_f64(ag.dk[:48, 0]), r_dk, "dk")
+    check_grad(to_f64(ag.dv[:48, 0]), r_dv, "dv")

@@ -97,11 +97,22 @@ def test_attention_kernels_vs_fp64(case):
         assert not to_f64(dk[g])[pad].any() and not to_f64(dv[g])[pad].any()
 
 
+def _recipe_lse(wl, inp, table):
+    """fp64 LSE of every head when attention is fed the bf16 rotated Q, K of
+    the fp32 recipe with `table` (the GPU's actual attention inputs)."""
+    pos, doc = O.positions_docs(wl.S, 1, inp.cu)
+    qr = O.bf16_to_f64(O.rope_recipe_bf16(inp.q, pos, table))
+    kr = O.bf16_to_f64(O.rope_recipe_bf16(inp.k, pos, table))
+    _, lse = O.attention_fwd(qr, kr, O.bf16_to_f64(inp.v), doc, 1.0 / math.sqrt(wl.D))
+    return lse
+
+
 @pytest.mark.parametrize("case", SMALL)
 def test_pipeline_vs_full_sequence(case):
     wl, inp = _setup(case, seed=1)
+    table = O.rope_table_f32(wl.S_pad, wl.D, wl.rope_base)
     ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
-                          rope_base=wl.rope_base)
+                          rope_base=wl.rope_base, rope_table=table)
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     dq, dk, dv = ua.step(q, k, v, do)
     ua.check()
@@ -114,12 +125,16 @@ def test_pipeline_vs_full_sequence(case):
     check_grad(to_f64(dq)[:S], ref["dq"], "dq")
     check_grad(to_f64(dk)[:S], ref["dk"], "dk")
     check_grad(to_f64(dv)[:S], ref["dv"], "dv")
-    loss = float(ua.loss(do))
+    # loss = sum(O * dO) over the valid rows, from the GPU's O (host arithmetic)
+    loss = float((to_f64(ua.o)[:S] * f(inp.do)).sum())
     assert abs(loss - ref["loss"]) <= 1e-2 * float(np.abs(ref["o"] * f(inp.do)).sum())
     lse = ua.lse.cpu().numpy().astype(np.float64).reshape(wl.Hq, wl.S_pad)[:, :S]
+    # against exact RoPE, LSE moves by the bf16 rounding of the rotated Q, K
     nq = np.linalg.norm(f(inp.q), axis=-1).max()     # rotation keeps norms
     nk = np.linalg.norm(f(inp.k), axis=-1).max()
     check_lse(lse, ref["lse"], lse_tol_end_to_end(nq, nk, 1.0 / math.sqrt(wl.D)))
+    # against the recipe-rotated bf16 Q, K the GPU attends to: 1e-3
+    check_lse(lse, _recipe_lse(wl, inp, table))
     # outputs past S (padding) are zero
     assert not to_f64(ua.o)[S:].any() and not to_f64(dq)[S:].any()
 
@@ -138,21 +153,25 @@ def test_attention_is_deterministic():
 # --------------------------------------------------------------- full sizes
 
 def _full_case(name):
+    """The full-size workload through the pipeline, with the oracle's RoPE
+    table (bitwise the library's up to rare one-ulp entries), so that the
+    recipe-rotated Q, K the oracle makes are exactly the GPU's."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl, 0)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
     ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
                           rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
-                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len)
+                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len,
+                          rope_table=orc.table())
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     ua.step(q, k, v, do)
     ua.check()
-    return wl, inp, ua
+    return wl, inp, ua, orc
 
 
 @pytest.mark.parametrize("name", ["sp8_120k", "thd64k", "long32k_pad", "qwen8k"])
 def test_full_workload_sampled(name):
-    wl, inp, ua = _full_case(name)
-    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
+    wl, inp, ua, orc = _full_case(name)
     rng = np.random.default_rng(5)
     S = wl.S
     rows = np.unique(np.concatenate([[0, 1, 127, 128, S // 2, S - 1], rng.integers(0, S, 10)]))
@@ -176,6 +195,9 @@ def test_full_workload_sampled(name):
     nk = m * np.linalg.norm(O.bf16_to_f64(inp.k), axis=-1).max()
     check_lse(np.concatenate(got_l), np.concatenate(ref_l),
               lse_tol_end_to_end(nq, nk, 1.0 / math.sqrt(wl.D)))
+    # 1e-3 against fp64 attention of the recipe-rotated bf16 Q, K
+    check_lse(np.concatenate(got_l), np.concatenate([orc.lse_rows_recipe(h, rows)
+                                                     for h in heads]))
     # dK/dV at the last rows of a document: only queries at or after them
     # see those keys, so the oracle needs just those query rows
     ends = [S] if inp.cu is None else [int(inp.cu[-1]), int(inp.cu[3])]
@@ -202,3 +224,32 @@ def test_padded_matches_unpadded_long():
     for a, b in zip(*outs):
         fa, fb = a.float(), b.float()
         assert (fa - fb).abs().max().item() <= 2e-2 * max(1.0, fb.abs().max().item())
+
+
+def _first_keys_case(name):
+    """(KV heads, first key, end of the longest document) of a workload."""
+    wl = WORKLOADS[name]
+    if wl.thd:
+        from ulysses_sequence_attention_usp_gb300.inputs import cu_seqlens, doc_lengths
+        cu = cu_seqlens(doc_lengths(wl.S))
+        d = int(np.argmax(np.diff(cu)))
+        return wl, [0, wl.Hkv - 1], int(cu[d]), int(cu[d + 1])
+    return wl, ([0] if wl.S > 100000 else [0, wl.Hkv - 1]), 0, wl.S
+
+
+@pytest.mark.parametrize("name", ["long32k_pad", "thd64k",
+                                  pytest.param("sp8_120k", marks=pytest.mark.slow)])
+def test_full_workload_first_keys(name):
+    """dK/dV of the first 48 keys of the longest document: every later query
+    row of the document sees them, so the key-stationary pass runs its
+    longest loop there (at 120K, 938 query tiles x 4 query heads accumulated
+    in TMEM).  The oracle needs each of those rows' LSE and delta, i.e. the
+    whole causal forward of the group's query heads, evaluated over row
+    chunks in worker processes."""
+    wl, kvs, a, e = _first_keys_case(name)
+    _, inp, ua, orc = _full_case(name)
+    keys = np.arange(a, a + 48)
+    for kh in kvs:
+        r_dk, r_dv = orc.dkv_keys(kh, keys, np.arange(a, e))
+        check_grad(to_f64(ua.dk[a:a + 48, kh]), r_dk, "dk")
+        check_grad(to_f64(ua.dv[a:a + 48, kh]), r_dv, "dv")

@@ -81,18 +81,19 @@ def test_bidirectional_pipeline_vs_full_sequence(case):
 def test_bidirectional_full_size_packed_sampled():
     wl = WORKLOADS["thd64k"]
     inp = make_inputs(wl, 0)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl, causal=False)
     ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
-                          rope_base=wl.rope_base, causal=False)
+                          rope_base=wl.rope_base, causal=False, rope_table=orc.table())
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     ua.step(q, k, v, do)
     ua.check()
-    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl, causal=False)
     rng = np.random.default_rng(6)
     S = wl.S
     rows = np.unique(np.concatenate([[0, 1, 127, 128, S // 2, S - 1], rng.integers(0, S, 10)]))
     lse = ua.lse.reshape(wl.Hq, wl.S_pad)
     got_o, ref_o, got_l, ref_l, got_dq, ref_dq = [], [], [], [], [], []
-    for h in sorted({0, wl.Hq - 1, int(rng.integers(0, wl.Hq))}):
+    heads = sorted({0, wl.Hq - 1, int(rng.integers(0, wl.Hq))})
+    for h in heads:
         r_o, r_l = orc.fwd_rows(h, rows)
         got_o.append(to_f64(ua.o[rows, h]))
         ref_o.append(r_o)
@@ -106,9 +107,21 @@ def test_bidirectional_full_size_packed_sampled():
     nk = np.linalg.norm(O.bf16_to_f64(inp.k), axis=-1).max()
     check_lse(np.concatenate(got_l), np.concatenate(ref_l),
               lse_tol_end_to_end(nq, nk, 1.0 / math.sqrt(wl.D)))
+    # 1e-3 against fp64 attention of the recipe-rotated bf16 Q, K
+    check_lse(np.concatenate(got_l), np.concatenate([orc.lse_rows_recipe(h, rows)
+                                                     for h in heads]))
     # dK/dV of a whole short document: every query of that document sees it
     a, b = int(inp.cu[3]), int(inp.cu[4])
     for kh in sorted({0, wl.Hkv - 1}):
         r_dk, r_dv = orc.dkv_tail(kh, a, b, q_lo=a)
         check_grad(to_f64(ua.dk[a:b, kh]), r_dk, "dk")
         check_grad(to_f64(ua.dv[a:b, kh]), r_dv, "dv")
+    # dK/dV of the first 48 keys of the longest document (13 083 rows): every
+    # query row of the document sees them, the longest key-stationary loop
+    d = int(np.argmax(np.diff(inp.cu)))
+    a, b = int(inp.cu[d]), int(inp.cu[d + 1])
+    keys = np.arange(a, a + 48)
+    for kh in sorted({0, wl.Hkv - 1}):
+        r_dk, r_dv = orc.dkv_keys(kh, keys, np.arange(a, b))
+        check_grad(to_f64(ua.dk[a:a + 48, kh]), r_dk, "dk")
+        check_grad(to_f64(ua.dv[a:a + 48, kh]), r_dv, "dv")

@@ -119,6 +119,45 @@ def test_seq_to_head_120k_yarn_sampled_rows():
                  f=wl.yarn_factor, L=wl.yarn_orig_ctx, rope_len=wl.rope_len)
 
 
+def _rows_120k(S, seed):
+    """Sampled rows of the 120K workload: shard edges, rows past the
+    repack's grid-stride threshold (152*64 blocks x 8 rows = 77 824) and
+    random rows."""
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 14999, 15000, 77823, 77824, 77825, 2 * 77824 - 1, S - 2, S - 1]
+    return np.unique(np.concatenate([fixed, rng.integers(0, S, 3000),
+                                     rng.integers(77824, S, 1000)]))
+
+
+def test_seq_to_head_120k_yarn_k_sampled_rows():
+    wl = WORKLOADS["sp8_120k"]
+    _repack_case(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, None, "k", 1, rows=_rows_120k(wl.S, 1),
+                 base=wl.rope_base, f=wl.yarn_factor, L=wl.yarn_orig_ctx, rope_len=wl.rope_len)
+
+
+@pytest.mark.parametrize("which,mode", [("q", -1), ("k", -1), ("v", 0)])
+def test_head_to_seq_120k_sampled_rows(which, mode):
+    # the inverse all-to-all of the gradients at full size, in the launch
+    # configuration of the benchmark (grid-stride loop beyond 77 824 rows)
+    wl = WORKLOADS["sp8_120k"]
+    H = wl.Hq if which == "q" else wl.Hkv
+    S, P, D = wl.S, wl.P, wl.D
+    d = _dims(S, P, wl.Hq, wl.Hkv, D)
+    table = O.rope_table_f32(wl.rope_len, D, wl.rope_base, wl.yarn_factor, wl.yarn_orig_ctx)
+    pos, _ = O.positions_docs(S, P)
+    xh = normal_bf16((P, S, H // P, D), 15, "do")
+    out = torch.empty((S, H, D), dtype=torch.bfloat16, device="cuda")
+    B.usp_head_to_seq(d, to_dev(xh), H, torch.from_numpy(pos.astype(np.int32)).cuda(),
+                      torch.from_numpy(table).cuda(), wl.rope_len, mode, out)
+    torch.cuda.synchronize()
+    rows = _rows_120k(S, 2)
+    got = out[torch.from_numpy(rows).cuda()]
+    want = np.ascontiguousarray(xh[:, rows].transpose(1, 0, 2, 3).reshape(len(rows), H, D))
+    if mode != 0:
+        want = O.rope_recipe_bf16(want, pos[rows], table, inverse=mode < 0)
+    assert np.array_equal(to_bits(got), want)
+
+
 @pytest.mark.parametrize("D,mode", [(128, -1), (128, 0), (64, -1), (64, 1)])
 def test_head_to_seq_bit_exact(D, mode):
     S, P, H = 1000, 4, 8

@@ -60,3 +60,19 @@ def test_both_arms_print_the_same_config_keys():
         assert c["workload"] == "sp8_120k" and c["S"] == 120000 and c["ring"] == ring
         assert ("all-gather" in c["shards"]) == (cp == "allgather")
         assert ("zigzag" in c["shards"]) == zz
+
+
+def test_both_arms_lines_share_the_config():
+    # both arms build their JSON line from bench.base_line, so `config` is the
+    # same dict for the same flags (the GPU arm's L2 note is a separate key)
+    import types
+    wl = WORKLOADS["sp8_120k"]
+    a = types.SimpleNamespace(cp="ulysses", bidirectional=False, zigzag=False, ring=1,
+                              steps=5, warmup=3)
+    gpu = bench.base_line(a, wl, 1, 3.5e5, 339.0, "bf16")
+    ref = dict(impl="reference", **bench.base_line(a, wl, 1, 10.0, 1.2e7, "f64"))
+    assert gpu["config"] == ref["config"] and "l2" not in gpu["config"]
+    for k in ("metric", "unit", "higher_is_better", "scaling", "n_gpus", "steps", "warmup"):
+        assert gpu[k] == ref[k]
+    src = open(bench.__file__).read()
+    assert src.count("base_line(args, wl,") == 3      # the definition and one call per arm
