@@ -246,33 +246,42 @@ def workload_config(args, wl, world=1):
                             f"replicas x{world} (P={wl.P} virtual shards per GPU)")}
 
 
+def base_line(args, wl, world, value, ms_per_step, dtype):
+    """The keys both arms print, with the same `config` for the same flags."""
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic", "config": workload_config(args, wl, world)}
+
+
 def run_reference(args, wl, inp):
     """--impl reference: the oracle, timed on host cores (rank 0 only)."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    times = []
+    times, raw = [], []
     causal = not args.bidirectional
     _, Sp, factor = oracle_sample(wl, inp, args.ref_seconds, causal=causal)
     for i in range(args.warmup + args.steps):
         dt, Sp, factor = oracle_sample(wl, inp, args.ref_seconds, fixed_rows=Sp, causal=causal)
         if i >= args.warmup:
             times.append(dt * factor)
+            raw.append(dt)
     full_s = statistics.median(times)
     value = wl.S / full_s
     sample = (f"oracle fwd+bwd of q head 0 / kv head 0 on the first {Sp} rows, "
               f"scaled by attended pairs x heads ({factor:.4g}x) to the full workload")
-    line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": full_s * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(args, wl, args.gpus),
+    line = dict(impl="reference", **base_line(args, wl, args.gpus, value, full_s * 1e3, "f64"))
+    line.update({
+        # a step is a bounded sample of the workload; its time is scaled up
+        "ms_per_step_extrapolated": True,
+        "ms_per_step_basis": (f"median over {args.steps} steps of the oracle's time on the "
+                              f"sample ({statistics.median(raw) * 1e3:.0f} ms) x {factor:.4g}"),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
-    }
+    })
     print(json.dumps(line), flush=True)
 
 
@@ -519,13 +528,9 @@ def run_usp(args, wl, inp):
         f_bwd_strict = 8.0 * wl.D * wl.Hq * pairs
         peak_t = peaks["bf16_tflops_sustained"]
         bwd_tf = f_bwd / t_bwd / 1e12
-        line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": dict(workload_config(args, wl, world),
-                           l2=l2_note(2 * (bq + bkv), l2)),
+        line = base_line(args, wl, world, value, step_s * 1e3, "bf16")
+        line.update({
+            "l2": l2_note(2 * (bq + bkv), l2),
             "roofline": {"kernel": "usp_attn_bwd (delta + dK/dV + dQ kernels)",
                          "bound": "tensor", "achieved": bwd_tf,
                          "peak": peak_t, "unit": "TFLOP/s", "frac": bwd_tf / peak_t,
@@ -556,7 +561,7 @@ def run_usp(args, wl, inp):
                               "steps' compute (two pipelines); Q/K/V go up before dO, O "
                               "comes down during the backward"},
             "clocks": clk,
-        }
+        })
         if world == 1 and not args.no_cpu_baseline:
             dt, Sp, factor = oracle_sample(wl, inp, args.cpu_seconds, causal=causal)
             line["cpu_baseline"] = {

@@ -46,7 +46,8 @@
  *   - Device-side waits are bounded.  A kernel that gives up records it in
  *     a device status word and exits; usp_device_status() reports it.
  *   - Calls keep no state between invocations and may be issued from any
- *     host thread.
+ *     host thread (the library's per-process lookups -- device addresses of
+ *     its status word and scratch, the SM count -- are made race-free).
  */
 #ifndef USP_H_
 #define USP_H_
@@ -241,15 +242,23 @@ usp_status usp_attn_bwd(const usp_dims* dims, const void* q_h, const void* k_h,
  * Same arguments, results and errors as usp_attn_bwd, minus the workspace:
  * the scratch lives in one fixed 32 MiB device array inside the library
  * (held by every GPU that loads the library until the process exits).  The
- * call allocates nothing and calls no allocating routine.
+ * call allocates nothing and calls no allocating routine.  The results are
+ * bitwise those of usp_attn_bwd.
  *   - Limit: usp_attn_bwd_workspace(dims) must be <= 32 MiB, i.e.
  *     P * (Hq/P) * ceil(S_pad/128)*128 <= 4194304; larger problems return
  *     USP_ERR_UNSUPPORTED before anything touches the device.
  *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
- *   - All calls share the array.  Calls that overlap on the GPU (other
- *     streams, other host threads, other devices' calls are fine) race on it
- *     and give wrong gradients; order them on one stream.
+ *     that device current.  With CUDA's default lazy module loading that
+ *     first lookup is also what loads the library's backward module and
+ *     gives the array its 32 MiB of device memory, so make the first call
+ *     on each device before reserving the rest of the device's memory (or
+ *     run with CUDA_MODULE_LOADING=EAGER), and before any stream capture.
+ *   - All calls on one device share that device's array, which keeps the
+ *     previous call's contents (every entry a call reads, it first
+ *     rewrites).  Calls on the same device that overlap on the GPU --
+ *     whether issued on different streams or from different host threads --
+ *     race on the array and give wrong gradients: order them on one stream.
+ *     Calls on other devices use their own copy of the array.
  */
 usp_status usp_attn_bwd_noalloc(const usp_dims* dims, const void* q_h, const void* k_h,
                                 const void* v_h, const void* o_h, const float* lse,
@@ -258,15 +267,20 @@ usp_status usp_attn_bwd_noalloc(const usp_dims* dims, const void* q_h, const voi
 
 /* Bytes of workspace usp_attn_bwd needs for dims: two fp32 arrays of
  * P*(Hq/P) rows of ceil(S_pad/128)*128 entries (delta_t and LSE_t*log2(e)),
- * each rounded up to 256 bytes.  Returns 0 for invalid dims. */
+ * each rounded up to 256 bytes.  Returns 0 for invalid dims and SIZE_MAX
+ * when the size does not fit in size_t. */
 size_t usp_attn_bwd_workspace(const usp_dims* dims);
 
 /*
- * usp_head_to_seq -- the inverse all-to-all (head -> seq), used for O and
- * for the gradients; rope_mode -1 applies the inverse rotation so that dQ
- * and dK become gradients of the pre-RoPE inputs.  Same rounding and table
- * rules as usp_seq_to_head_rope.
- *   x_head [P][S_pad][H/P][D] bf16 -> x_seq [S_pad][H][D] bf16
+ * usp_head_to_seq -- the inverse all-to-all (head -> seq) that returns the
+ * attention output to sequence shards after local attention (SpecForge #728,
+ * Modifications), and carries the gradients back the same way; rope_mode -1
+ * applies the inverse rotation so that dQ and dK become gradients of the
+ * pre-RoPE inputs, which is what the gradient-parity criterion compares
+ * (SpecForge #728, Accuracy Test).  Same rounding and table rules as
+ * usp_seq_to_head_rope.
+ *   x_head [P][S_pad][H/P][D] bf16 -> x_seq [S_pad][H][D] bf16 (shard
+ *          layout of dims->zigzag), x_seq[t][g*H/P + j] = x_head[g][t][j]
  */
 usp_status usp_head_to_seq(const usp_dims* dims, const void* x_head, int32_t H,
                            const int32_t* pos, const float* rope_cs, int64_t rope_len,

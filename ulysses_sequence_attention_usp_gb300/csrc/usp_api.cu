@@ -22,18 +22,13 @@ void usp_count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_
 
 namespace {
 
-// Device address of g_status for the current device (looked up once per
-// device; the symbol lives in this translation unit).
+// Device address of g_status on the current device.  Looked up on every
+// call (a table lookup once the module is loaded), so nothing is cached
+// across host threads and an address never outlives its context.
 unsigned* status_word() {
-  static unsigned* cache[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (cache[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, usp::g_status) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<unsigned*>(p);
-  }
-  return cache[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, usp::g_status) != cudaSuccess) return nullptr;
+  return static_cast<unsigned*>(p);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "usp.h"
 
 namespace usp {
@@ -39,15 +41,28 @@ __device__ __forceinline__ void cta_coords(int n_tiles, int band, int& rank, int
 // band holds at least one CTA per SM, so that a band's heaviest tiles never
 // wait behind a whole band of other heads (the tail of a small problem),
 // while a large problem keeps one head per band.
-inline int cta_band(int n_tiles, int n_y) {
-  static int n_sm = 0;
-  if (n_sm == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        n_sm <= 0)
-      n_sm = 1;
+// SMs of the current device (the attribute query is cached per device in
+// atomics, so concurrent first calls from several host threads are benign).
+inline int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev >= 64) {
+    int n = 0;
+    return cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+                   n > 0 ? n : 1;
   }
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+inline int cta_band(int n_tiles, int n_y) {
+  const int n_sm = sm_count();
   int band = 1;
   while (band < n_y && (int64_t)band * n_tiles < n_sm) band *= 2;
   return band < n_y ? band : (n_y > 0 ? n_y : 1);

@@ -145,11 +145,6 @@ class UlyssesAttention:
         self.forward(q, k, v, stream)
         return self.backward(do, stream)
 
-    def loss(self, do) -> torch.Tensor:
-        """sum(O * dO) over the valid rows, in fp32 on the device (reporting
-        only; not part of the hot path)."""
-        return (self.o[:self.S].float() * do.float()).sum()
-
     def check(self, stream=None):
         B.usp_device_status(stream)
 
