@@ -1,9 +1,9 @@
 """Benchmark of the USP attention hot path (one JSON line on rank 0).
 
 A step is one full pass of the path over one synthetic batch:
-  pad/shard Q,K,V -> seq->head all-to-all with RoPE (Q,K) and plain (V)
-  -> causal GQA attention forward -> head->seq (O)
-  -> pad/shard dO -> seq->head (dO) -> attention backward
+  positions/documents -> seq->head all-to-all with RoPE (Q,K) and plain (V),
+  padding rows written as zeros -> causal GQA attention forward
+  -> head->seq (O) -> seq->head (dO) -> attention backward
   -> head->seq (dQ, dK with inverse RoPE; dV).
 The default workload is the 120 000-token SP8 layer (Hq/Hkv/D = 32/8/128,
 YaRN RoPE to 131 072).  Inputs (0.98 GB for Q alone) are larger than L2, so
@@ -352,21 +352,35 @@ def run_usp(args, wl, inp):
         ]
         rep_bytes = {"rope_qk": 2 * (bq + bkv) + 2 * tab, "rope_grads": 2 * (bq + bkv) + 2 * tab}
     else:
-        stages = [
-            ("pad_qkv", lambda: (
+        # the same calls as UlyssesAttention.forward/backward: in the
+        # contiguous layout the all-to-all reads the unpadded inputs and
+        # writes padding rows as zeros, so the first stage only emits
+        # positions and documents; zigzag shards are padded copies first
+        if args.zigzag:
+            src = (ua.q_seq, ua.k_seq, ua.v_seq, ua.do_seq)
+            first = ("pad_qkv", lambda: (
                 B.usp_pad_shard(d, q, wl.Hq, ua.q_seq, ua.pos, ua.doc, st),
                 B.usp_pad_shard(d, k, wl.Hkv, ua.k_seq, None, None, st),
-                B.usp_pad_shard(d, v, wl.Hkv, ua.v_seq, None, None, st))),
+                B.usp_pad_shard(d, v, wl.Hkv, ua.v_seq, None, None, st)))
+        else:
+            src = (q, k, v, do)
+            first = ("positions", lambda: B.usp_pad_shard(d, None, 0, None, ua.pos, ua.doc, st))
+        stages = [
+            first,
             ("repack_qkv", lambda: (
-                B.usp_seq_to_head_rope(d, ua.q_seq, wl.Hq, ua.pos, ua.rope, ua.rope_len, 1,
+                B.usp_seq_to_head_rope(d, src[0], wl.Hq, ua.pos, ua.rope, ua.rope_len, 1,
                                        ua.q_h, st),
-                B.usp_seq_to_head_rope(d, ua.k_seq, wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1,
+                B.usp_seq_to_head_rope(d, src[1], wl.Hkv, ua.pos, ua.rope, ua.rope_len, 1,
                                        ua.k_h, st),
-                B.usp_seq_to_head_rope(d, ua.v_seq, wl.Hkv, None, None, 0, 0, ua.v_h, st))),
+                B.usp_seq_to_head_rope(d, src[2], wl.Hkv, None, None, 0, 0, ua.v_h, st))),
             ("attn_fwd", lambda: ua.attention_forward(st)),     # one launch, or the ring steps
             ("repack_o", lambda: B.usp_head_to_seq(d, ua.o_h, wl.Hq, None, None, 0, 0, ua.o, st)),
-            ("pad_do", lambda: B.usp_pad_shard(d, do, wl.Hq, ua.do_seq, None, None, st)),
-            ("repack_do", lambda: B.usp_seq_to_head_rope(d, ua.do_seq, wl.Hq, None, None, 0, 0,
+        ]
+        if args.zigzag:
+            stages.append(("pad_do", lambda: B.usp_pad_shard(d, do, wl.Hq, ua.do_seq, None, None,
+                                                             st)))
+        stages += [
+            ("repack_do", lambda: B.usp_seq_to_head_rope(d, src[3], wl.Hq, None, None, 0, 0,
                                                          ua.do_h, st)),
             ("attn_bwd", lambda: B.usp_attn_bwd(d, ua.q_h, ua.k_h, ua.v_h, ua.o_h, ua.lse,
                                                 ua.do_h, ua.doc, ua.dq_h, ua.dk_h, ua.dv_h,

@@ -67,7 +67,9 @@ typedef enum {
   USP_ERR_HEADS_NOT_DIVISIBLE = 2,  /* P does not divide Hq or Hkv, or Hkv does not divide Hq */
   USP_ERR_UNSUPPORTED = 3,          /* e.g. D not in {64,128} */
   USP_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed */
-  USP_ERR_TIMEOUT = 5               /* a device-side wait gave up (see usp_device_status) */
+  USP_ERR_TIMEOUT = 5,              /* a device-side wait gave up (see usp_device_status) */
+  USP_ERR_OUT_OF_BOUNDS = 6         /* a debug build's index guard stopped an access
+                                       outside a buffer's extent (see usp_debug_build) */
 } usp_status;
 
 /* Problem description shared by all calls. */
@@ -135,7 +137,12 @@ usp_status usp_pad_shard(const usp_dims* dims, const void* x, int32_t H,
  * with RoPE at absolute positions.
  *
  *   x_seq  [S_pad][H][D] bf16 (shard layout of dims->zigzag) -> x_head
- *          [P][S_pad][H/P][D] bf16 in global row order
+ *          [P][S_pad][H/P][D] bf16 in global row order.  Padding rows
+ *          (global rows t >= S) are zero by definition: their head-layout
+ *          rows are written as zeros and x_seq is never read there.  In the
+ *          contiguous layout x_seq may therefore be the caller's unpadded
+ *          [S][H][D] tensor itself (no usp_pad_shard copy is needed; that
+ *          call then only emits pos/doc).
  *   rope_mode 0: plain permutation (V, dO); pos/rope_cs may be NULL.
  *   rope_mode 1: rotate every (d, d+D/2) pair of row t by the table entry
  *                at pos[t]; -1 rotates by the negated angle.
@@ -302,10 +309,23 @@ usp_status usp_rope_table(int64_t n_pos, int32_t D, double base, double yarn_fac
 /*
  * usp_device_status -- synchronise `stream`, then report and clear the
  * device status word: USP_ERR_TIMEOUT if a kernel's bounded wait gave up,
+ * USP_ERR_OUT_OF_BOUNDS if a debug build's index guard fired,
  * USP_ERR_INVALID_ARG if a kernel met a position outside the RoPE table,
  * USP_ERR_CUDA if the stream reported an error, else USP_OK.
  */
 usp_status usp_device_status(void* stream);
+
+/*
+ * usp_debug_build -- 1 if this library was built with index guards: every
+ * global-memory index a kernel computes is checked against the extent that
+ * usp_dims implies for its buffer, and an out-of-range index sets a status
+ * bit (reported as USP_ERR_OUT_OF_BOUNDS) and skips the access instead of
+ * reading or writing out of bounds; 0 for the release build.  (The kind of
+ * fault this catches -- an out-of-range RoPE table gather that fired a
+ * device-side assert -- is the one basetenlabs/Megatron-LM PR #7, Purpose,
+ * describes.)
+ */
+int usp_debug_build(void);
 
 /*
  * usp_selftest_bounded_wait -- diagnostic for the failure-detection path:

@@ -59,7 +59,9 @@ def test_pad_shard_in_place_zeroes_tail_only():
 
 
 def _repack_case(S, P, Hq, Hkv, D, cu, which, mode, rows=None, base=1.0e4, f=1.0, L=0,
-                 rope_len=0):
+                 rope_len=0, unpadded=False):
+    """seq -> head of a padded [S_pad][H][D] source, or (unpadded=True) of the
+    caller's [S][H][D] tensor, which the library reads only at valid rows."""
     H = Hq if which == "q" else Hkv
     d = _dims(S, P, Hq, Hkv, D, cu)
     S_pad = O.padded_len(S, P)
@@ -67,10 +69,10 @@ def _repack_case(S, P, Hq, Hkv, D, cu, which, mode, rows=None, base=1.0e4, f=1.0
     table = O.rope_table_f32(n_pos, D, base, f, L)
     x = O.shard_pad(normal_bf16((S, H, D), 11, which), P)
     pos, _ = O.positions_docs(S, P, None if cu is None else np.array(cu))
-    out = torch.empty((P, S_pad, H // P, D), dtype=torch.bfloat16, device="cuda")
+    out = torch.full((P, S_pad, H // P, D), 3.0, dtype=torch.bfloat16, device="cuda")
     tpos = torch.from_numpy(pos.astype(np.int32)).cuda()
     ttab = torch.from_numpy(table).cuda()
-    B.usp_seq_to_head_rope(d, to_dev(x), H, tpos, ttab, n_pos, mode, out)
+    B.usp_seq_to_head_rope(d, to_dev(x[:S] if unpadded else x), H, tpos, ttab, n_pos, mode, out)
     torch.cuda.synchronize()
     got = to_bits(out)
     if rows is None:
@@ -99,6 +101,19 @@ def test_seq_to_head_small_ragged(case):
         _repack_case(*case, which, mode)
 
 
+@pytest.mark.parametrize("case", [
+    (30, 4, 8, 4, 128, None),
+    (777, 4, 8, 4, 64, [0, 100, 101, 401, 777]),
+    (1, 8, 8, 8, 128, None),
+    (32766, 8, 32, 8, 128, None),
+])
+def test_seq_to_head_reads_unpadded_source(case):
+    # padding rows come out as zeros without a padded copy of the input: the
+    # source tensor holds only the S valid rows
+    for which, mode in (("q", 1), ("k", 1), ("v", 0)):
+        _repack_case(*case, which, mode, unpadded=True)
+
+
 @pytest.mark.parametrize("name", ["qwen8k", "long32k_pad", "thd64k"])
 def test_seq_to_head_full_workloads(name):
     wl = WORKLOADS[name]
@@ -124,7 +139,7 @@ def _rows_120k(S, seed):
     repack's grid-stride threshold (152*64 blocks x 8 rows = 77 824) and
     random rows."""
     rng = np.random.default_rng(seed)
-    fixed = [0, 1, 14999, 15000, 77823, 77824, 77825, 2 * 77824 - 1, S - 2, S - 1]
+    fixed = [0, 1, 14999, 15000, 77823, 77824, 77825, S - 2, S - 1]
     return np.unique(np.concatenate([fixed, rng.integers(0, S, 3000),
                                      rng.integers(77824, S, 1000)]))
 

@@ -54,18 +54,21 @@ __device__ __forceinline__ int doc_of(const int32_t* cu, int n_docs, int64_t t) 
   return lo;
 }
 
+// x holds n_valid_vec 16-byte vectors (S rows), y n_total_vec (S_pad rows).
 __global__ void __launch_bounds__(256) pad_shard_kernel(
     const uint4* __restrict__ x, uint4* __restrict__ y, int64_t n_valid_vec,
     int64_t n_total_vec, int inplace, int32_t* __restrict__ pos, int32_t* __restrict__ doc,
     const int32_t* __restrict__ cu, int n_docs, int64_t S, int64_t S_pad, int64_t row_vec,
-    int64_t zz_chunk, int P) {
+    int64_t zz_chunk, int P, unsigned* status) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   if (zz_chunk == 0) {
     for (int64_t i = i0; i < n_total_vec; i += stride) {
+      if (!usp::in_bounds(i, 1, n_total_vec, status)) continue;
       if (i < n_valid_vec) {
-        if (!inplace) st_stream(y + i, ld_stream(x + i));
+        if (!inplace && usp::in_bounds(i, 1, n_valid_vec, status))
+          st_stream(y + i, ld_stream(x + i));
       } else {
         st_stream(y + i, zero);
       }
@@ -74,7 +77,10 @@ __global__ void __launch_bounds__(256) pad_shard_kernel(
     for (int64_t i = i0; i < n_total_vec; i += stride) {
       const int64_t r = i / row_vec, c = i - r * row_vec;
       const int64_t t = zz_global(r, zz_chunk, P);
-      st_stream(y + i, t < S ? ld_stream(x + t * row_vec + c) : zero);
+      const int64_t xi = t * row_vec + c;
+      if (!usp::in_bounds(i, 1, n_total_vec, status)) continue;
+      st_stream(y + i, t < S && usp::in_bounds(xi, 1, n_valid_vec, status) ? ld_stream(x + xi)
+                                                                           : zero);
     }
   }
   if (pos == nullptr && doc == nullptr) return;
@@ -83,8 +89,9 @@ __global__ void __launch_bounds__(256) pad_shard_kernel(
     int64_t start = 0;
     if (cu != nullptr) {
       d = doc_of(cu, n_docs, t);
-      start = __ldg(cu + d);
+      if (usp::in_bounds(d, 1, n_docs + 1, status)) start = __ldg(cu + d);
     }
+    if (!usp::in_bounds(t, 1, S_pad, status)) continue;
     if (pos) pos[t] = (int32_t)(t - start);
     if (doc) doc[t] = t < S ? d : -1;
   }
@@ -95,10 +102,16 @@ __global__ void __launch_bounds__(256) pad_shard_kernel(
 // threads; thread `sub` owns pairs [8*sub, 8*sub+8): elements d = 8*sub..+7
 // and their rotation partners d + D/2.  32/(D/16) heads are processed per
 // step and kUnroll steps are loaded before any is stored.
+// Seq -> head: padding rows (global t >= S) are zero by definition, so the
+// kernel takes zeros for them instead of reading the source (which
+// therefore only needs its valid rows: the caller's unpadded tensor serves
+// directly in the contiguous layout, and no padding copy is made).  The
+// zeros still go through the rotation, so a padding row's output is
+// bitwise what rotating a zero-filled row gives (signed zeros included).
 template <int D, int MODE, bool TO_HEAD>
 __global__ void __launch_bounds__(256) repack_kernel(
     const bf16* __restrict__ src, bf16* __restrict__ dst, const int32_t* __restrict__ pos,
-    const float* __restrict__ cs, int64_t rope_len, int64_t S_pad, int H, int hp,
+    const float* __restrict__ cs, int64_t rope_len, int64_t S, int64_t S_pad, int H, int hp,
     unsigned* status, int64_t zz_chunk, int P) {
   constexpr int TPH = D / 16;
   constexpr int HPI = 32 / TPH;
@@ -108,20 +121,28 @@ __global__ void __launch_bounds__(256) repack_kernel(
   const int slot = lane / TPH;
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  // element extents usp_dims implies (index guards of debug builds): the
+  // sequence side holds S rows, or all S_pad rows of zigzag shards
+  const int64_t n_seq = (TO_HEAD && zz_chunk == 0 ? S : S_pad) * H * (int64_t)D;
+  const int64_t n_head = S_pad * H * (int64_t)D;
+  const int64_t n_src = TO_HEAD ? n_seq : n_head, n_dst = TO_HEAD ? n_head : S_pad * H * (int64_t)D;
 
   for (int64_t t = warp; t < S_pad; t += nwarps) {
     const int64_t srow = zz_row(t, zz_chunk, P);   // row of t in the sharded buffer
+    const bool pad_row = TO_HEAD && t >= S;         // zeros, nothing read
     float c[8], s[8];
     bool zero_row = false;
     if (MODE != 0) {
-      const int p = __ldg(pos + t);
+      const int p = usp::in_bounds(t, 1, S_pad, status) ? __ldg(pos + t) : -1;
       if (p < 0 || (int64_t)p >= rope_len) {
         if (lane == 0) usp::set_status(status, usp::kErrRopeRange);
         zero_row = true;
 #pragma unroll
         for (int i = 0; i < 8; ++i) { c[i] = 0.f; s[i] = 0.f; }
       } else {
-        const float4* tp = reinterpret_cast<const float4*>(cs + ((int64_t)p * (D / 2) + 8 * sub) * 2);
+        const int64_t toff = ((int64_t)p * (D / 2) + 8 * sub) * 2;
+        const bool tab_ok = usp::in_bounds(toff, 16, rope_len * D, status);
+        const float4* tp = reinterpret_cast<const float4*>(cs + (tab_ok ? toff : 0));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float4 v = __ldg(tp + i);
@@ -146,8 +167,15 @@ __global__ void __launch_bounds__(256) repack_kernel(
           const int64_t head_off = (((int64_t)g * S_pad + t) * hp + j) * (int64_t)D;
           const bf16* sp = src + (TO_HEAD ? seq_off : head_off);
           doff[u] = TO_HEAD ? head_off : seq_off;
-          lo[u] = ld_stream(sp + 8 * sub);
-          hi[u] = ld_stream(sp + D / 2 + 8 * sub);
+          const int64_t so = (TO_HEAD ? seq_off : head_off) + 8 * sub;
+          if (pad_row || !usp::in_bounds(so, 8, n_src, status) ||
+              !usp::in_bounds(so + D / 2, 8, n_src, status)) {
+            lo[u] = make_uint4(0, 0, 0, 0);
+            hi[u] = lo[u];
+          } else {
+            lo[u] = ld_stream(sp + 8 * sub);
+            hi[u] = ld_stream(sp + D / 2 + 8 * sub);
+          }
         }
       }
 #pragma unroll
@@ -172,8 +200,11 @@ __global__ void __launch_bounds__(256) repack_kernel(
           if (zero_row) { a = make_uint4(0, 0, 0, 0); b = a; }
         }
         bf16* dp = dst + doff[u];
-        st_stream(dp + 8 * sub, a);
-        st_stream(dp + D / 2 + 8 * sub, b);
+        if (usp::in_bounds(doff[u] + 8 * sub, 8, n_dst, status) &&
+            usp::in_bounds(doff[u] + D / 2 + 8 * sub, 8, n_dst, status)) {
+          st_stream(dp + 8 * sub, a);
+          st_stream(dp + D / 2 + 8 * sub, b);
+        }
       }
     }
   }
@@ -188,18 +219,18 @@ int repack_grid(int64_t S_pad) {
 
 template <int D, bool TO_HEAD>
 cudaError_t launch_mode(int mode, const bf16* src, bf16* dst, const int32_t* pos,
-                        const float* cs, int64_t rope_len, int64_t S_pad, int H, int hp,
-                        unsigned* status, int64_t zz, int P, cudaStream_t st) {
+                        const float* cs, int64_t rope_len, int64_t S, int64_t S_pad, int H,
+                        int hp, unsigned* status, int64_t zz, int P, cudaStream_t st) {
   const int grid = repack_grid(S_pad);
   if (mode == 0)
-    repack_kernel<D, 0, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp,
-                                                       status, zz, P);
+    repack_kernel<D, 0, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad, H,
+                                                       hp, status, zz, P);
   else if (mode > 0)
-    repack_kernel<D, 1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H, hp,
-                                                       status, zz, P);
+    repack_kernel<D, 1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad, H,
+                                                       hp, status, zz, P);
   else
-    repack_kernel<D, -1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S_pad, H,
-                                                        hp, status, zz, P);
+    repack_kernel<D, -1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad,
+                                                        H, hp, status, zz, P);
   usp_count_launches(1);
   return cudaGetLastError();
 }
@@ -218,7 +249,8 @@ cudaError_t usp_launch_pad_shard(const usp::Geometry& g, const void* x, int H, v
   if (blocks < 1) blocks = 1;
   pad_shard_kernel<<<(int)blocks, 256, 0, st>>>(
       reinterpret_cast<const uint4*>(x), reinterpret_cast<uint4*>(x_seq), n_valid, n_total,
-      x == x_seq ? 1 : 0, pos, doc, cu, n_docs, g.S, g.S_pad, row_vec, g.zz_chunk, g.P);
+      x == x_seq ? 1 : 0, pos, doc, cu, n_docs, g.S, g.S_pad, row_vec, g.zz_chunk, g.P,
+      g.status);
   usp_count_launches(1);
   return cudaGetLastError();
 }
@@ -231,12 +263,12 @@ cudaError_t usp_launch_repack(const usp::Geometry& g, const void* src, int H, co
   bf16* d = reinterpret_cast<bf16*>(dst);
   const int64_t zz = g.zz_chunk;
   if (g.D == 128)
-    return to_head ? launch_mode<128, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H,
-                                            hp, g.status, zz, g.P, st)
-                   : launch_mode<128, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H,
-                                             hp, g.status, zz, g.P, st);
-  return to_head ? launch_mode<64, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H, hp,
-                                         g.status, zz, g.P, st)
-                 : launch_mode<64, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S_pad, H,
-                                          hp, g.status, zz, g.P, st);
+    return to_head ? launch_mode<128, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S, g.S_pad,
+                                            H, hp, g.status, zz, g.P, st)
+                   : launch_mode<128, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S,
+                                             g.S_pad, H, hp, g.status, zz, g.P, st);
+  return to_head ? launch_mode<64, true>(rope_mode, s, d, pos, rope_cs, rope_len, g.S, g.S_pad, H,
+                                         hp, g.status, zz, g.P, st)
+                 : launch_mode<64, false>(rope_mode, s, d, pos, rope_cs, rope_len, g.S, g.S_pad,
+                                          H, hp, g.status, zz, g.P, st);
 }

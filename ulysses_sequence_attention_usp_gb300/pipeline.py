@@ -5,10 +5,17 @@ runs the hot path by calling the library's entry points in order
 (SpecForge PR #728 "feat(dspark): add Ulysses sequence parallel training",
 Modifications):
 
-forward:   pad/shard Q,K,V  ->  seq->head all-to-all (+RoPE on Q,K)
+forward:   positions/documents (+ shard copies for the zigzag layout)
+           ->  seq->head all-to-all (+RoPE on Q,K), padding rows as zeros
            ->  local causal GQA attention per head group  ->  head->seq (O)
-backward:  pad/shard dO  ->  seq->head (dO)  ->  attention backward
+backward:  seq->head (dO)  ->  attention backward
            ->  head->seq (dQ, dK with the inverse rotation; dV)
+
+In the contiguous shard layout the all-to-all reads the caller's unpadded
+tensors directly: padding rows are zero by definition, so the library
+writes them without reading anything and no padded copy is made.  The
+zigzag layout reorders rows, so there the inputs are first copied into
+padded zigzag shards.
 
 PyTorch provides device memory and the stream only; every step runs in the
 library's kernels.
@@ -65,8 +72,9 @@ class UlyssesAttention:
         e = lambda *s, dt=bf: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
         self.pos = e(Sp, dt=torch.int32)
         self.doc = e(Sp, dt=torch.int32)
-        self.q_seq, self.k_seq, self.v_seq = e(Sp, Hq, D), e(Sp, Hkv, D), e(Sp, Hkv, D)
-        self.do_seq = e(Sp, Hq, D)
+        if self.zigzag:   # padded zigzag shards of the inputs
+            self.q_seq, self.k_seq, self.v_seq = e(Sp, Hq, D), e(Sp, Hkv, D), e(Sp, Hkv, D)
+            self.do_seq = e(Sp, Hq, D)
         self.q_h, self.k_h, self.v_h = e(P, Sp, hq, D), e(P, Sp, hkv, D), e(P, Sp, hkv, D)
         self.do_h, self.o_h = e(P, Sp, hq, D), e(P, Sp, hq, D)
         self.lse = e(P, hq, Sp, dt=torch.float32)
@@ -89,14 +97,16 @@ class UlyssesAttention:
         for n, t, h in (("q", q, self.Hq), ("k", k, self.Hkv), ("v", v, self.Hkv)):
             _check_input(n, t, self.S, h, self.D, self.device)
         d, st = self.dims, stream
-        B.usp_pad_shard(d, q, self.Hq, self.q_seq, self.pos, self.doc, st)
-        B.usp_pad_shard(d, k, self.Hkv, self.k_seq, None, None, st)
-        B.usp_pad_shard(d, v, self.Hkv, self.v_seq, None, None, st)
-        B.usp_seq_to_head_rope(d, self.q_seq, self.Hq, self.pos, self.rope, self.rope_len, 1,
-                               self.q_h, st)
-        B.usp_seq_to_head_rope(d, self.k_seq, self.Hkv, self.pos, self.rope, self.rope_len, 1,
-                               self.k_h, st)
-        B.usp_seq_to_head_rope(d, self.v_seq, self.Hkv, None, None, 0, 0, self.v_h, st)
+        if self.zigzag:
+            B.usp_pad_shard(d, q, self.Hq, self.q_seq, self.pos, self.doc, st)
+            B.usp_pad_shard(d, k, self.Hkv, self.k_seq, None, None, st)
+            B.usp_pad_shard(d, v, self.Hkv, self.v_seq, None, None, st)
+            q, k, v = self.q_seq, self.k_seq, self.v_seq
+        else:
+            B.usp_pad_shard(d, None, 0, None, self.pos, self.doc, st)
+        B.usp_seq_to_head_rope(d, q, self.Hq, self.pos, self.rope, self.rope_len, 1, self.q_h, st)
+        B.usp_seq_to_head_rope(d, k, self.Hkv, self.pos, self.rope, self.rope_len, 1, self.k_h, st)
+        B.usp_seq_to_head_rope(d, v, self.Hkv, None, None, 0, 0, self.v_h, st)
         self.attention_forward(st)
         B.usp_head_to_seq(d, self.o_h, self.Hq, None, None, 0, 0, self.o, st)
         self._forward_done = True
@@ -130,8 +140,10 @@ class UlyssesAttention:
             raise RuntimeError("backward before forward")
         _check_input("do", do, self.S, self.Hq, self.D, self.device)
         d, st = self.dims, stream
-        B.usp_pad_shard(d, do, self.Hq, self.do_seq, None, None, st)
-        B.usp_seq_to_head_rope(d, self.do_seq, self.Hq, None, None, 0, 0, self.do_h, st)
+        if self.zigzag:
+            B.usp_pad_shard(d, do, self.Hq, self.do_seq, None, None, st)
+            do = self.do_seq
+        B.usp_seq_to_head_rope(d, do, self.Hq, None, None, 0, 0, self.do_h, st)
         B.usp_attn_bwd(d, self.q_h, self.k_h, self.v_h, self.o_h, self.lse, self.do_h, self.doc,
                        self.dq_h, self.dk_h, self.dv_h, self.ws, self.ws_bytes, st)
         B.usp_head_to_seq(d, self.dq_h, self.Hq, self.pos, self.rope, self.rope_len, -1,
