@@ -13,19 +13,22 @@ import os
 import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libusp.so")
+# USP_DEBUG_BOUNDS=1 loads the build with index guards (build(debug=True))
+DEBUG = os.environ.get("USP_DEBUG_BOUNDS") == "1"
+LIB_PATH = os.path.join(_HERE, "_build_debug" if DEBUG else "_build", "libusp.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "usp.h")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"USP CUDA library not built ({LIB_PATH} missing); run "
-        "`python -m ulysses_sequence_attention_usp_gb300.build`")
+        "`python -m ulysses_sequence_attention_usp_gb300.build" + (" -d`" if DEBUG else "`"))
 
 _lib = ctypes.CDLL(LIB_PATH)
 
 USP_OK = 0
 STATUS_NAMES = {0: "USP_OK", 1: "USP_ERR_INVALID_ARG", 2: "USP_ERR_HEADS_NOT_DIVISIBLE",
-                3: "USP_ERR_UNSUPPORTED", 4: "USP_ERR_CUDA", 5: "USP_ERR_TIMEOUT"}
+                3: "USP_ERR_UNSUPPORTED", 4: "USP_ERR_CUDA", 5: "USP_ERR_TIMEOUT",
+                6: "USP_ERR_OUT_OF_BOUNDS"}
 
 
 class UspError(RuntimeError):
@@ -71,6 +74,8 @@ _lib.usp_status_string.argtypes = [ctypes.c_int]
 _lib.usp_status_string.restype = ctypes.c_char_p
 _lib.usp_abi_version.argtypes = []
 _lib.usp_abi_version.restype = ctypes.c_int
+_lib.usp_debug_build.argtypes = []
+_lib.usp_debug_build.restype = ctypes.c_int
 _lib.usp_launch_count.argtypes = []
 _lib.usp_launch_count.restype = ctypes.c_uint64
 
@@ -210,6 +215,10 @@ def usp_abi_version() -> int:
 
 def usp_launch_count() -> int:
     return int(_lib.usp_launch_count())
+
+
+def usp_debug_build() -> bool:
+    return bool(_lib.usp_debug_build())
 
 
 def raw_call(name, *args):

@@ -756,7 +756,9 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
                                                     const float* __restrict__ lse,
                                                     float* __restrict__ delta,
                                                     float* __restrict__ lse2, int64_t S_pad,
-                                                    int64_t S_ws, int hq, int64_t n_rows) {
+                                                    int64_t S_ws, int hq, int64_t n_rows,
+                                                    unsigned* status) {
+  const int64_t n_ws = (n_rows / S_pad) * S_ws;    // entries of each workspace vector
   {
     const int64_t extra = S_ws - S_pad;
     const int64_t n_extra = (n_rows / S_pad) * extra;     // (P*hq) rows
@@ -764,6 +766,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
          i += (int64_t)gridDim.x * blockDim.x) {
       const int64_t rr = i / extra;
       const int64_t idx = rr * S_ws + S_pad + (i - rr * extra);
+      if (!usp::in_bounds(idx, 1, n_ws, status)) continue;
       delta[idx] = 0.f;
       lse2[idx] = -INFINITY;
     }
@@ -776,7 +779,7 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
   for (int64_t base = w0 * RPW; base < n_rows; base += nw * RPW) {
     const int64_t row = base + lane / LPR;    // row = (g*S_pad + t)*hq + j
     float s = 0.f;
-    if (row < n_rows) {
+    if (row < n_rows && usp::in_bounds(row * D + 8 * (lane % LPR), 8, n_rows * D, status)) {
       const uint4 a = __ldcs(reinterpret_cast<const uint4*>(o + row * D) + lane % LPR);
       const uint4 b = __ldcs(reinterpret_cast<const uint4*>(dout + row * D) + lane % LPR);
       const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
@@ -796,8 +799,10 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
       const int j = (int)(row - gt * hq);
       const int64_t g = gt / S_pad, t = gt - g * S_pad;
       const int64_t li = (g * hq + j) * S_ws + t;
+      const int64_t lj = (g * hq + j) * S_pad + t;
+      if (!usp::in_bounds(li, 1, n_ws, status) || !usp::in_bounds(lj, 1, n_rows, status)) continue;
       delta[li] = -s;
-      const float x = lse[(g * hq + j) * S_pad + t];
+      const float x = lse[lj];
       lse2[li] = x == -INFINITY ? -INFINITY : -(x * kLog2e);
     }
   }
@@ -814,8 +819,8 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
   const int64_t n_rows = (int64_t)g.P * g.S_pad * g.hq;
   int64_t blocks = (n_rows * (D / 8) * 1 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
-  delta_kernel<D><<<(int)(blocks < 1 ? 1 : blocks), 256, 0, st>>>(o, dout, lse, delta, lse2,
-                                                                 g.S_pad, prm.S_ws, g.hq, n_rows);
+  delta_kernel<D><<<(int)(blocks < 1 ? 1 : blocks), 256, 0, st>>>(
+      o, dout, lse, delta, lse2, g.S_pad, prm.S_ws, g.hq, n_rows, prm.status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   constexpr int smem_kv = CfgKV<D>::SMEM, smem_q = CfgQ<D>::SMEM;
@@ -836,13 +841,21 @@ cudaError_t launch_all(const usp::Geometry& g, const CUtensorMap& mq, const CUte
 }  // namespace
 
 // Workspace: delta and lse2, each [P][hq][S_ws] fp32 with S_ws = S_pad
-// rounded up to a multiple of BT.
+// rounded up to a multiple of BT.  Sizes that do not fit in size_t give
+// SIZE_MAX, which no workspace (and no fixed scratch) satisfies.
 static int64_t ws_row(const usp::Geometry& g) { return (g.S_pad + BT - 1) / BT * BT; }
 static size_t vec_bytes(const usp::Geometry& g) {
-  const size_t n = (size_t)g.P * g.hq * ws_row(g) * sizeof(float);
+  const uint64_t rows = (uint64_t)g.P * (uint64_t)g.hq;
+  const uint64_t row_bytes = (uint64_t)ws_row(g) * sizeof(float);
+  const uint64_t cap = (SIZE_MAX / 2 - 255);
+  if (row_bytes != 0 && rows > cap / row_bytes) return SIZE_MAX;
+  const size_t n = (size_t)(rows * row_bytes);
   return ((n + 255) / 256) * 256;
 }
-size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g) { return 2 * vec_bytes(g); }
+size_t usp_attn_bwd_ws_bytes(const usp::Geometry& g) {
+  const size_t v = vec_bytes(g);
+  return v == SIZE_MAX ? SIZE_MAX : 2 * v;
+}
 
 cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const void* k,
                                 const void* v, const void* o, const float* lse,
@@ -896,20 +909,16 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 size_t usp_noalloc_scratch_capacity() { return kNoAllocScratchBytes; }
 
-// Device address of the scratch array on the current device.  The first
-// call on a device looks it up (with that device current) and caches it.
+// Device address of the scratch array on the current device, looked up
+// with that device current on every call: the first lookup on a device
+// loads this module there (under lazy loading) and with it the array; later
+// lookups are a table read.  Nothing is cached, so concurrent first calls
+// from several host threads do not race and no address outlives its
+// context.
 cudaError_t usp_noalloc_scratch(void** ptr) {
-  static void* cache[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (cache[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    cache[dev] = p;
-  }
-  *ptr = cache[dev];
+  *ptr = p;
   return cudaSuccess;
 }

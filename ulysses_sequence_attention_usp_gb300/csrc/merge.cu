@@ -18,7 +18,7 @@ template <int D>
 __global__ void __launch_bounds__(256) lse_merge_kernel(
     float* __restrict__ o_acc, float* __restrict__ lse_acc, const bf16* __restrict__ o_part,
     const float* __restrict__ lse_part, int first, bf16* __restrict__ o_out, int64_t S_pad,
-    int hq, int64_t n_rows) {
+    int hq, int64_t n_rows, unsigned* status) {
   constexpr int TPR = D / 4;                    // threads per row
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t stride = ((int64_t)gridDim.x * blockDim.x) / TPR;
@@ -29,6 +29,10 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(
     const int j = (int)(row - gt * hq);
     const int64_t g = gt / S_pad, t = gt - g * S_pad;
     const int64_t li = (g * hq + j) * S_pad + t;
+    // index guards of debug builds: LSE arrays hold n_rows entries, O arrays n_rows*D
+    if (!usp::in_bounds(li, 1, n_rows, status) ||
+        !usp::in_bounds(row * D + 4 * sub, 4, n_rows * D, status))
+      continue;
     const float lb = __ldg(lse_part + li);
     const float la = first ? -INFINITY : lse_acc[li];
     const float mx = fmaxf(la, lb);
@@ -77,10 +81,10 @@ cudaError_t usp_launch_lse_merge(const usp::Geometry& g, float* o_acc, float* ls
   bf16* ob = reinterpret_cast<bf16*>(o_out);
   if (g.D == 128)
     lse_merge_kernel<128><<<(int)blocks, 256, 0, st>>>(o_acc, lse_acc, pb, lse_part, first, ob,
-                                                       g.S_pad, g.hq, n_rows);
+                                                       g.S_pad, g.hq, n_rows, g.status);
   else
     lse_merge_kernel<64><<<(int)blocks, 256, 0, st>>>(o_acc, lse_acc, pb, lse_part, first, ob,
-                                                      g.S_pad, g.hq, n_rows);
+                                                      g.S_pad, g.hq, n_rows, g.status);
   usp_count_launches(1);
   return cudaGetLastError();
 }

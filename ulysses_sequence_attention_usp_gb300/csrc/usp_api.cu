@@ -102,6 +102,14 @@ extern "C" {
 
 int usp_abi_version(void) { return USP_ABI_VERSION; }
 
+int usp_debug_build(void) {
+#ifdef USP_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 uint64_t usp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* usp_status_string(usp_status s) {
@@ -112,6 +120,7 @@ const char* usp_status_string(usp_status s) {
     case USP_ERR_UNSUPPORTED: return "unsupported configuration";
     case USP_ERR_CUDA: return "CUDA error";
     case USP_ERR_TIMEOUT: return "device-side wait timed out";
+    case USP_ERR_OUT_OF_BOUNDS: return "index outside a buffer's extent (debug build)";
   }
   return "unknown status";
 }
@@ -127,6 +136,7 @@ usp_status usp_pad_shard(const usp_dims* dims, const void* x, int32_t H, void* x
   if (((uintptr_t)pos & 3u) || ((uintptr_t)doc & 3u)) return USP_ERR_INVALID_ARG;
   if (g.zz_chunk > 0 && x != nullptr && x == x_seq) return USP_ERR_INVALID_ARG;
   if (g.S_pad == 0) return USP_OK;
+  if ((g.status = status_word()) == nullptr) return USP_ERR_CUDA;
   return cuda_status(usp_launch_pad_shard(g, x, H, H > 0 ? x_seq : nullptr, pos, doc,
                                           dims->cu_seqlens, dims->n_docs,
                                           (cudaStream_t)stream));
@@ -205,6 +215,7 @@ usp_status usp_lse_merge(const usp_dims* dims, float* o_acc, float* lse_acc, con
   if (o_out != nullptr && !aligned16(o_out)) return USP_ERR_INVALID_ARG;
   if (first != 0 && first != 1) return USP_ERR_INVALID_ARG;
   if (g.S_pad == 0) return USP_OK;
+  if ((g.status = status_word()) == nullptr) return USP_ERR_CUDA;
   return cuda_status(usp_launch_lse_merge(g, o_acc, lse_acc, o_part, lse_part, first, o_out,
                                           (cudaStream_t)stream));
 }
@@ -315,6 +326,7 @@ usp_status usp_device_status(void* stream) {
   if (word != 0 && cudaMemcpyToSymbol(usp::g_status, &zero, sizeof(zero)) != cudaSuccess)
     return USP_ERR_CUDA;
   if (word & usp::kErrTimeout) return USP_ERR_TIMEOUT;
+  if (word & usp::kErrIndex) return USP_ERR_OUT_OF_BOUNDS;
   if (word & usp::kErrRopeRange) return USP_ERR_INVALID_ARG;
   return USP_OK;
 }

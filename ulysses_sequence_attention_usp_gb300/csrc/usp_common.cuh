@@ -12,12 +12,30 @@
 namespace usp {
 
 // Device status word: bit 0 = a bounded wait gave up, bit 1 = a position
-// fell outside the RoPE table.  Kernels receive its address as an argument;
+// fell outside the RoPE table, bit 2 = a debug build's index guard stopped
+// an out-of-range access.  Kernels receive its address as an argument;
 // usp_device_status reports and clears it.
-enum : unsigned { kErrTimeout = 1u, kErrRopeRange = 2u };
+enum : unsigned { kErrTimeout = 1u, kErrRopeRange = 2u, kErrIndex = 4u };
 
 __device__ __forceinline__ void set_status(unsigned* word, unsigned bits) {
   if (word) atomicOr(word, bits);
+}
+
+// Index guard of every global-memory access the kernels compute themselves
+// (TMA tiles are clipped by their tensor maps).  Builds with
+// USP_DEBUG_BOUNDS check that the `count` elements starting at element
+// `idx` lie inside a buffer of `n` elements -- the extent usp_dims implies
+// for that buffer -- and otherwise record kErrIndex and tell the caller to
+// skip the access.  Release builds compile the guard to `true`.
+__device__ __forceinline__ bool in_bounds(int64_t idx, int64_t count, int64_t n,
+                                          unsigned* status) {
+#ifdef USP_DEBUG_BOUNDS
+  if (idx < 0 || count < 0 || idx > n - count) {
+    set_status(status, kErrIndex);
+    return false;
+  }
+#endif
+  return true;
 }
 
 // Order of the CTAs of an attention launch over n_tiles row tiles x n_y head
