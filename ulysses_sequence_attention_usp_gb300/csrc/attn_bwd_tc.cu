@@ -98,17 +98,25 @@ struct Params {
   int causal;            // 0: every key of a row's document is visible
   float scale, scale_log2;
   unsigned* status;
+  int n_docs;              // entries of cu - 1 (index guards of debug builds)
+  int64_t n_q, n_kv, n_ws; // elements of q/dq, of dk/dv, of each workspace vector
 };
 
-__device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
-  if (t >= p.S) return -1;
+// Document of row t (-1 for a pad row); debug builds check the indices into
+// doc and cu_seqlens and treat an out-of-range document id as a pad row.
+__device__ __forceinline__ int doc_index(const Params& p, int64_t t) {
+  if (t >= p.S || !usp::in_bounds(t, 1, p.S_pad, p.status)) return -1;
   const int d = __ldg(p.doc + t);
+  if (d < 0 || (p.cu && !usp::in_bounds(d, 2, p.n_docs + 1, p.status))) return -1;
+  return d;
+}
+__device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
+  const int d = doc_index(p, t);
   if (d < 0) return -1;
   return p.cu ? (int64_t)__ldg(p.cu + d) : 0;
 }
 __device__ __forceinline__ int64_t doc_end_of(const Params& p, int64_t t) {
-  if (t >= p.S) return -1;
-  const int d = __ldg(p.doc + t);
+  const int d = doc_index(p, t);
   if (d < 0) return -1;
   return p.cu ? (int64_t)__ldg(p.cu + d + 1) : p.S;
 }
@@ -519,7 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // lse2 next to the Q tile, delta next to the dO tile
             const int64_t off = ((int64_t)g * p.hq + jk * G + it % G) * p.S_ws + tq0 +
                                 (int64_t)(it / G) * BT;
-            return (w == 0 ? p.nlse2 : p.ndelta) + off;
+            // debug builds: an out-of-range vector is reported and replaced
+            // by the first one, so that the copy still completes its barrier
+            const bool in = usp::in_bounds(off, BT, p.n_ws, p.status);
+            return (w == 0 ? p.nlse2 : p.ndelta) + (in ? off : 0);
           });
     }
   } else if (warp == 1) {
@@ -580,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // epilogue: the left half writes dV, the right half dK
     const bool have = ok && n_it > 0;          // warp-uniform
-    bf16* row = (half == 0 ? p.dv : p.dk) + (((int64_t)g * p.S_pad + u) * p.hkv + jk) * D;
+    const int64_t row_off = (((int64_t)g * p.S_pad + u) * p.hkv + jk) * D;
+    bf16* row = (half == 0 ? p.dv : p.dk) + row_off;
     const uint32_t acc = 256 + half * D;
     const float f = half == 0 ? 1.f : p.scale;
 #pragma unroll
@@ -592,7 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
       }
-      if (u < p.S_pad) store_row32(row + c * 32, v, f);
+      if (u < p.S_pad && usp::in_bounds(row_off + c * 32, 32, p.n_kv, p.status))
+        store_row32(row + c * 32, v, f);
     }
   }
   __syncwarp();
@@ -674,8 +687,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     float nlse2 = -INFINITY, ndl = 0.f;
     if (ds >= 0) {
       const int64_t li = ((int64_t)g * p.hq + jq) * p.S_ws + t;
-      nlse2 = __ldg(p.nlse2 + li);
-      ndl = __ldg(p.ndelta + li);
+      if (usp::in_bounds(li, 1, p.n_ws, p.status)) {
+        nlse2 = __ldg(p.nlse2 + li);
+        ndl = __ldg(p.ndelta + li);
+      }
     }
     const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, kDqT0);
     const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, kDqT1);
@@ -685,11 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       uint32_t qw[32];
       const bool mine = D == 128 || half == 0;     // D = 64: the left group holds the row
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + (((int64_t)g * p.S_pad + t) * p.hq + jq) * D + (mine ? 64 * half : 0));
+      const int64_t q_off = (((int64_t)g * p.S_pad + t) * p.hq + jq) * D + (mine ? 64 * half : 0);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + q_off);
+      const bool rd = t < p.S_pad && mine && usp::in_bounds(q_off, 64, p.n_q, p.status);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint4 v = (t < p.S_pad && mine) ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        const uint4 v = rd ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
         qw[4 * i] = v.x; qw[4 * i + 1] = v.y; qw[4 * i + 2] = v.z; qw[4 * i + 3] = v.w;
       }
       if (D == 128 || half == 0)
@@ -722,7 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_after_sync();
     }
     const bool have = ok && n_kv > 0;
-    bf16* row = p.dq + (((int64_t)g * p.S_pad + t) * p.hq + jq) * D;
+    const int64_t row_off = (((int64_t)g * p.S_pad + t) * p.hq + jq) * D;
+    bf16* row = p.dq + row_off;
 #pragma unroll
     for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
       uint32_t v[32];
@@ -732,7 +749,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0u;
       }
-      if (t < p.S_pad) store_row32(row + c * 32, v, ds >= 0 ? p.scale : 0.f);
+      if (t < p.S_pad && usp::in_bounds(row_off + c * 32, 32, p.n_q, p.status))
+        store_row32(row + c * 32, v, ds >= 0 ? p.scale : 0.f);
     }
   }
   __syncwarp();
@@ -891,6 +909,10 @@ cudaError_t usp_launch_attn_bwd(const usp::Geometry& g, const void* q, const voi
   prm.scale = g.scale;
   prm.scale_log2 = g.scale * kLog2e;
   prm.status = g.status;
+  prm.n_docs = g.n_docs;
+  prm.n_q = (int64_t)g.P * g.S_pad * g.hq * g.D;
+  prm.n_kv = (int64_t)g.P * g.S_pad * g.hkv * g.D;
+  prm.n_ws = (int64_t)g.P * g.hq * prm.S_ws;
   const bf16* ob = reinterpret_cast<const bf16*>(o);
   const bf16* db = reinterpret_cast<const bf16*>(dout);
   if (g.D == 128) return launch_all<128>(g, mq, mk, mv, mdo, prm, ob, db, lse, delta, lse2, st);

@@ -67,6 +67,8 @@ struct Params {
   int64_t k_lo, k_hi;     // key window: only rows [k_lo, k_hi) are keys
   float scale_log2;
   unsigned* status;
+  int n_docs;             // entries of cu - 1 (index guards of debug builds)
+  int64_t n_o, n_lse;     // elements of o and lse
 };
 
 struct Bars {
@@ -80,16 +82,23 @@ struct Bars {
   int abort;
 };
 
-__device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
-  if (t >= p.S) return -1;
+// Document of row t (-1 for a pad row).  Debug builds check the index into
+// doc and the document's two cu_seqlens entries, and treat a row whose
+// document id lies outside cu_seqlens as a pad row.
+__device__ __forceinline__ int doc_index(const Params& p, int64_t t) {
+  if (t >= p.S || !usp::in_bounds(t, 1, p.S_pad, p.status)) return -1;
   const int d = __ldg(p.doc + t);
+  if (d < 0 || (p.cu && !usp::in_bounds(d, 2, p.n_docs + 1, p.status))) return -1;
+  return d;
+}
+__device__ __forceinline__ int64_t doc_start_of(const Params& p, int64_t t) {
+  const int d = doc_index(p, t);
   if (d < 0) return -1;
   return p.cu ? (int64_t)__ldg(p.cu + d) : 0;
 }
 // One past the last row of t's document (-1 for a pad row).
 __device__ __forceinline__ int64_t doc_end_of(const Params& p, int64_t t) {
-  if (t >= p.S) return -1;
-  const int d = __ldg(p.doc + t);
+  const int d = doc_index(p, t);
   if (d < 0) return -1;
   return p.cu ? (int64_t)__ldg(p.cu + d + 1) : p.S;
 }
@@ -376,16 +385,16 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           w[i] = tc::pack_bf16(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv);
-        if (t < p.S_pad) {
+        if (t < p.S_pad && usp::in_bounds(orow + c * 32 - p.o, 32, p.n_o, p.status)) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
             dst[q4] = make_uint4(w[4 * q4], w[4 * q4 + 1], w[4 * q4 + 2], w[4 * q4 + 3]);
         }
       }
-      if (t < p.S_pad)
-        p.lse[((int64_t)g * p.hq + j) * p.S_pad + t] =
-            has ? (m + __log2f(l)) * kLn2 : -INFINITY;
+      const int64_t li = ((int64_t)g * p.hq + j) * p.S_pad + t;
+      if (t < p.S_pad && usp::in_bounds(li, 1, p.n_lse, p.status))
+        p.lse[li] = has ? (m + __log2f(l)) * kLn2 : -INFINITY;
     }
   }
 
@@ -478,6 +487,9 @@ cudaError_t usp_launch_attn_fwd(const usp::Geometry& g, const void* q, const voi
   prm.k_hi = k_hi;
   prm.scale_log2 = g.scale * kLog2e;
   prm.status = g.status;
+  prm.n_docs = g.n_docs;
+  prm.n_o = (int64_t)g.P * g.S_pad * g.hq * g.D;
+  prm.n_lse = (int64_t)g.P * g.hq * g.S_pad;
   if (g.D == 128)
     return nh == 2 ? launch_fwd<128, 2>(g, mq, mk, mv, prm, st)
                    : launch_fwd<128, 1>(g, mq, mk, mv, prm, st);

@@ -66,6 +66,7 @@ usp_status geometry(const usp_dims* d, usp::Geometry* g) {
   g->hkv = d->Hkv / d->P;
   g->G = d->Hq / d->Hkv;
   g->scale = d->scale > 0.f ? d->scale : (float)(1.0 / sqrt((double)d->D));
+  g->n_docs = d->cu_seqlens != nullptr ? d->n_docs : 0;
   g->status = nullptr;
   return USP_OK;
 }

@@ -92,6 +92,7 @@ struct Geometry {
   int P, Hq, Hkv, D, hq, hkv, G;
   int causal;            // 1: keys u <= t of the document; 0: the whole document
   int64_t zz_chunk;      // zigzag chunk C = S_pad/(2P); 0 for contiguous shards
+  int n_docs;            // documents in cu_seqlens (0: one document, no cu_seqlens)
   float scale;
   unsigned* status;   // device address of the status word of the current device
 };
