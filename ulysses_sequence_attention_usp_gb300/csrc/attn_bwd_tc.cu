@@ -14,8 +14,9 @@
 //                 Hq/Hkv query heads of the group and the query tiles that
 //                 see these keys, accumulating dV and dK in TMEM:
 //                   S^T  = K Q^T,  dP^T = V dO^T        (SS MMA)
-//                   P^T, dS^T computed per key row by 128 threads, written
-//                   as bf16 over S^T and dP^T in TMEM
+//                   P^T, dS^T computed per key row by 128 threads, both
+//                   written as bf16 over S^T's TMEM region; S^T and dP^T
+//                   swap regions every iteration
 //                   dV  += P^T dO,  dK += dS^T Q        (TS MMA)
 //   dq_kernel     one CTA per 128 query rows of one query head; loops over
 //                 key tiles:  S = Q K^T, dP = dO V^T (SS), dS over S (bf16),
@@ -70,7 +71,8 @@ struct Bars {
   uint64_t ring_empty[4];  // per stage: the MMAs reading it completed
   uint64_t sd_full;       // dq: S and dP of the iteration computed; dkdv: S^T computed
   uint64_t dp_full;       // dkdv: dP^T computed
-  uint64_t consumed;      // dq: both elementwise groups read S and dP (256 arrivals)
+  uint64_t consumed;      // dq: both elementwise groups read S and dP; dkdv: they read
+                          // dP^T (256 arrivals)
   uint64_t q_ready;       // dq: the Q tile is in TMEM (256 arrivals)
   uint64_t p_full[2];     // dkdv: P^T published ([0]), dS^T published ([1]);
                           // dq: dS written ([0]); 256 arrivals each
@@ -201,20 +203,24 @@ __device__ __forceinline__ void mma_tile_ss(uint32_t d_tmem, uint32_t f, uint32_
   }
 }
 
-// dK/dV MMA issuer.  Iteration `it` streams ring tiles Q (R0) and dO (R1):
-//   S^T = K Q^T (T0) -> sd_full,   dP^T = V dO^T (T1) -> dp_full     (SS)
-//   dV += P^T dO  once P^T is published over T0                     (TS)
-//   dK += dS^T Q  once dS^T is published over T1                    (TS)
-// Issue order in steady state:  dV(it), S^T(it+1), dK(it), dP^T(it+1).
-// S^T(it+1) may overwrite T0 once dV(it) has read P^T (done[0]) and runs
-// while the elementwise groups compute dS^T(it); dP^T(it+1) may overwrite
-// T1 once dK(it) has read dS^T (done[1]) and runs while they compute
-// P^T(it+1).  Each wait thus has an MMA queued behind it.
+// dK/dV MMA issuer.  Iteration `it` streams ring tiles Q (R0) and dO (R1).
+// Two 128-column TMEM regions take turns: S^T(it) goes to region R (T0 for
+// even it, T1 for odd) and dP^T(it) to the other region O.  The elementwise
+// groups write P^T(it) as bf16 over the first 16 columns of each 32-column
+// chunk of R and dS^T(it) over the other 16, so once they have read dP^T(it)
+// out of O, O is free for S^T(it+1):
+//   dV(it) += P^T(it) dO(it)   once P^T(it) is published   (TS, A from R)
+//   S^T(it+1) = K Q^T  -> O    once dP^T(it) has been read (`consumed`)
+//   dK(it) += dS^T(it) Q(it)   once dS^T(it) is published  (TS, A from R)
+//   dP^T(it+1) = V dO^T -> R   once dK(it), and with it dV(it), completed
+// S^T(it+1) thus waits for no MMA to finish, so the P^T phase of it+1 (the
+// longer elementwise phase) runs while dK(it) and dP^T(it+1) execute; only
+// dP^T(it+1) still waits for the pipe, since dK(it) reads R.
 template <int D>
 __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatile int* abort,
                                               uint32_t tmem, int n_it) {
   using C = CfgKV<D>;
-  constexpr uint32_t T0 = 0, T1 = 128, A0 = 256, A1 = 256 + D;
+  constexpr uint32_t A0 = 256, A1 = 256 + D;
   constexpr uint32_t id_acc = tc::idesc_bf16(128, D, true);
   const uint32_t fix = tc::smem_u32(smem + C::FIX_OFF);
   const uint32_t ring = tc::smem_u32(smem + C::RING_OFF);
@@ -222,30 +228,30 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
             tc::mbar_wait_warp(&bars->ring_full[0], 0, abort);
   if (ok) {
     tc::fence_after_sync();
-    mma_tile_ss<C>(tmem + T0, fix, ring);
+    mma_tile_ss<C>(tmem + 0, fix, ring);
     tc::mma_commit_w(&bars->sd_full);
-    mma_tile_ss<C>(tmem + T1, fix + C::TILE, ring + C::TILE);
+    mma_tile_ss<C>(tmem + 128, fix + C::TILE, ring + C::TILE);
     tc::mma_commit_w(&bars->dp_full);
   }
   for (int it = 0; ok && it < n_it; ++it) {
     const int st = it % C::NST2, nst = (it + 1) % C::NST2;
     const int s0 = 2 * st, s1 = 2 * st + 1, n0 = 2 * nst, n1 = 2 * nst + 1;
+    const uint32_t R = (it & 1) ? 128u : 0u, O = 128u - R;
     const bool more = it + 1 < n_it;
     // dV(it) += P^T(it) dO(it)
     if (!(ok = tc::mbar_wait_warp(&bars->p_full[0], it & 1, abort))) break;
     tc::fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-      tc::mma_ts_w(tmem + A0, tmem + T0 + 32 * (kk >> 1) + 8 * (kk & 1),
+      tc::mma_ts_w(tmem + A0, tmem + R + 32 * (kk >> 1) + 8 * (kk & 1),
                  tc::desc_sw128(ring + s1 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
-    tc::mma_commit_w(&bars->done[0]);
-    // S^T(it+1) once dV(it) has read P^T(it)
+    // S^T(it+1) into O once dP^T(it) has been read out of it
     if (more) {
+      if (!(ok = tc::mbar_wait_warp(&bars->consumed, it & 1, abort))) break;
       if (!(ok = tc::mbar_wait_warp(&bars->ring_full[nst], ((it + 1) / C::NST2) & 1, abort))) break;
-      if (!(ok = tc::mbar_wait_warp(&bars->done[0], it & 1, abort))) break;
       tc::fence_after_sync();
-      mma_tile_ss<C>(tmem + T0, fix, ring + n0 * C::TILE);
+      mma_tile_ss<C>(tmem + O, fix, ring + n0 * C::TILE);
       tc::mma_commit_w(&bars->sd_full);
     }
     // dK(it) += dS^T(it) Q(it)
@@ -253,16 +259,16 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
     tc::fence_after_sync();
 #pragma unroll
     for (int kk = 0; kk < BT / 16; ++kk)
-      tc::mma_ts_w(tmem + A1, tmem + T1 + 32 * (kk >> 1) + 8 * (kk & 1),
+      tc::mma_ts_w(tmem + A1, tmem + R + 16 + 32 * (kk >> 1) + 8 * (kk & 1),
                  tc::desc_sw128(ring + s0 * C::TILE + kk * 2048, C::BOX, 1024), id_acc,
                  (it > 0 || kk > 0) ? 1u : 0u);
     tc::mma_commit_w(&bars->done[1]);
     tc::mma_commit_w(&bars->ring_empty[st]);
-    // dP^T(it+1) once dK(it) has read dS^T(it)
+    // dP^T(it+1) into R once dV(it) and dK(it) have read P^T(it), dS^T(it)
     if (more) {
       if (!(ok = tc::mbar_wait_warp(&bars->done[1], it & 1, abort))) break;
       tc::fence_after_sync();
-      mma_tile_ss<C>(tmem + T1, fix + C::TILE, ring + n1 * C::TILE);
+      mma_tile_ss<C>(tmem + R, fix + C::TILE, ring + n1 * C::TILE);
       tc::mma_commit_w(&bars->dp_full);
     }
   }
@@ -342,11 +348,12 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
 
 // dK/dV elementwise work on half h (queries [64h, 64h+64)) of this thread's
 // key row, in two phases so that each overlaps an MMA:
-//   phase 1 (while dP^T is computed): P^T = exp2(S^T*sl2 - lse2[col]),
-//            written as bf16 over S^T and kept, as the same bf16 pairs, in
-//            32 registers;
-//   phase 2 (while dV is computed):   dS^T = P^T (dP^T - delta[col]),
-//            written as bf16 over dP^T.
+//   phase 1: P^T = exp2(S^T*sl2 - lse2[col]) from region R, written as bf16
+//            over R (first 16 columns of each 32-column chunk) and kept, as
+//            the same bf16 pairs, in 32 registers;
+//   phase 2: dS^T = P^T (dP^T - delta[col]) with dP^T read from region O
+//            (which the thread then reports `consumed`), written as bf16
+//            over R (last 16 columns of each chunk).
 // dS^T is thus formed from the bf16 P^T that dV is built from (a relative
 // change of at most 2^-9 per element, the size of the rounding dS^T gets
 // anyway).  The per-column lse2 and delta come in registers, negated (the
@@ -383,12 +390,17 @@ __device__ __forceinline__ void dkdv_phase_p(uint32_t tS, int h, int lo, int hi,
   }
 }
 
-__device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, int h, const float (&d2)[64],
-                                              const uint32_t (&pk)[32]) {
+__device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, uint32_t tS, int h,
+                                              const float (&d2)[64], const uint32_t (&pk)[32],
+                                              Bars* bars) {
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
     uint32_t dv[32];
     tc::tmem_ld_x32(tP + 64 * h + 32 * cc, dv);
+    if (cc == 1) {          // all of this thread's dP^T columns are read
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->consumed);
+    }
     uint32_t dw[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -401,7 +413,7 @@ __device__ __forceinline__ void dkdv_phase_ds(uint32_t tP, int h, const float (&
       tc::mul2(t0, t1, p0, p1, t0, t1);
       dw[i] = tc::pack_bf16(t0, t1);
     }
-    tc::tmem_st_x16(tP + 64 * h + 32 * cc, dw);
+    tc::tmem_st_x16(tS + 64 * h + 32 * cc + 16, dw);
   }
 }
 
@@ -542,8 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t u = u0 + r;
     const int64_t de = doc_end_of(p, u);         // queries [qs, de) see key u
     const int64_t qs = p.causal ? u : doc_start_of(p, u);
-    const uint32_t tS = tc::tmem_addr(tmem, quarter * 32, 0);
-    const uint32_t tP = tc::tmem_addr(tmem, quarter * 32, 128);
+    // the two TMEM regions that S^T and dP^T alternate between
+    const uint32_t tT0 = tc::tmem_addr(tmem, quarter * 32, 0);
+    const uint32_t tT1 = tc::tmem_addr(tmem, quarter * 32, 128);
     // per-query LSE*log2(e) (next to the Q tile) and delta (next to the dO
     // tile) of this half's 64 columns, staged by the producer
     const float* vec = reinterpret_cast<const float*>(smem + C::VEC_OFF) + 64 * half;
@@ -556,6 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; ok && it < n_it; ++it) {
       const int64_t t0 = tq0 + (int64_t)(it / p.G) * BT;
       const int s1 = 2 * (it % C::NST2) + 1;     // this stage's dO slot (delta)
+      const uint32_t tS = (it & 1) ? tT1 : tT0;  // S^T(it), then P^T, dS^T
+      const uint32_t tP = (it & 1) ? tT0 : tT1;  // dP^T(it)
       ok = tc::mbar_wait_warp(&bars->sd_full, it & 1, abort);
       if (!ok) break;
       tc::fence_after_sync();
@@ -573,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = tc::mbar_wait_warp(&bars->dp_full, it & 1, abort);
       if (!ok) break;
       tc::fence_after_sync();
-      dkdv_phase_ds(tP, half, d2, pk);
+      dkdv_phase_ds(tP, tS, half, d2, pk, bars);
       tc::tmem_wait_st();
       tc::fence_before_sync();
       tc::mbar_arrive(&bars->p_full[1]);
