@@ -98,17 +98,20 @@ __global__ void __launch_bounds__(256) pad_shard_kernel(
 }
 
 // ------------------------------------------------------------------ repack
-// One warp per token row t.  A head's D elements are covered by D/16
-// threads; thread `sub` owns pairs [8*sub, 8*sub+8): elements d = 8*sub..+7
-// and their rotation partners d + D/2.  32/(D/16) heads are processed per
-// step and kUnroll steps are loaded before any is stored.
+// One warp per R consecutive token rows.  A head's D elements are covered
+// by D/16 threads; thread `sub` owns pairs [8*sub, 8*sub+8): elements
+// d = 8*sub..+7 and their rotation partners d + D/2.  32/(D/16) heads are
+// processed per step and kUnroll steps (spread over the R rows) are loaded
+// before any is stored.  R = 2 for tensors with few heads, so that a warp
+// still has kUnroll loads in flight behind each row's dependent position
+// and table reads.
 // Seq -> head: padding rows (global t >= S) are zero by definition, so the
 // kernel takes zeros for them instead of reading the source (which
 // therefore only needs its valid rows: the caller's unpadded tensor serves
 // directly in the contiguous layout, and no padding copy is made).  The
 // zeros still go through the rotation, so a padding row's output is
 // bitwise what rotating a zero-filled row gives (signed zeros included).
-template <int D, int MODE, bool TO_HEAD>
+template <int D, int MODE, bool TO_HEAD, int R>
 __global__ void __launch_bounds__(256) repack_kernel(
     const bf16* __restrict__ src, bf16* __restrict__ dst, const int32_t* __restrict__ pos,
     const float* __restrict__ cs, int64_t rope_len, int64_t S, int64_t S_pad, int H, int hp,
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(256) repack_kernel(
   constexpr int TPH = D / 16;
   constexpr int HPI = 32 / TPH;
   constexpr int kUnroll = 4;
+  constexpr int UPR = kUnroll / R;               // load steps per row
   const int lane = threadIdx.x & 31;
   const int sub = lane % TPH;
   const int slot = lane / TPH;
@@ -127,48 +131,56 @@ __global__ void __launch_bounds__(256) repack_kernel(
   const int64_t n_head = S_pad * H * (int64_t)D;
   const int64_t n_src = TO_HEAD ? n_seq : n_head, n_dst = TO_HEAD ? n_head : S_pad * H * (int64_t)D;
 
-  for (int64_t t = warp; t < S_pad; t += nwarps) {
-    const int64_t srow = zz_row(t, zz_chunk, P);   // row of t in the sharded buffer
-    const bool pad_row = TO_HEAD && t >= S;         // zeros, nothing read
-    float c[8], s[8];
-    bool zero_row = false;
-    if (MODE != 0) {
-      const int p = usp::in_bounds(t, 1, S_pad, status) ? __ldg(pos + t) : -1;
-      if (p < 0 || (int64_t)p >= rope_len) {
-        if (lane == 0) usp::set_status(status, usp::kErrRopeRange);
-        zero_row = true;
+  for (int64_t tb = warp * R; tb < S_pad; tb += nwarps * R) {
+    int64_t srow[R];
+    bool pad_row[R], zero_row[R];
+    float c[R][8], s[R][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { c[i] = 0.f; s[i] = 0.f; }
-      } else {
-        const int64_t toff = ((int64_t)p * (D / 2) + 8 * sub) * 2;
-        const bool tab_ok = usp::in_bounds(toff, 16, rope_len * D, status);
-        const float4* tp = reinterpret_cast<const float4*>(cs + (tab_ok ? toff : 0));
+    for (int r = 0; r < R; ++r) {
+      const int64_t t = tb + r;
+      srow[r] = zz_row(t, zz_chunk, P);            // row of t in the sharded buffer
+      pad_row[r] = TO_HEAD && t >= S;              // zeros, nothing read
+      zero_row[r] = false;
+      if (MODE != 0 && t < S_pad) {
+        const int p = usp::in_bounds(t, 1, S_pad, status) ? __ldg(pos + t) : -1;
+        if (p < 0 || (int64_t)p >= rope_len) {
+          if (lane == 0) usp::set_status(status, usp::kErrRopeRange);
+          zero_row[r] = true;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 v = __ldg(tp + i);
-          c[2 * i] = v.x; s[2 * i] = v.y; c[2 * i + 1] = v.z; s[2 * i + 1] = v.w;
-        }
-        if (MODE < 0) {
+          for (int i = 0; i < 8; ++i) { c[r][i] = 0.f; s[r][i] = 0.f; }
+        } else {
+          const int64_t toff = ((int64_t)p * (D / 2) + 8 * sub) * 2;
+          const bool tab_ok = usp::in_bounds(toff, 16, rope_len * D, status);
+          const float4* tp = reinterpret_cast<const float4*>(cs + (tab_ok ? toff : 0));
 #pragma unroll
-          for (int i = 0; i < 8; ++i) s[i] = -s[i];
+          for (int i = 0; i < 4; ++i) {
+            const float4 v = __ldg(tp + i);
+            c[r][2 * i] = v.x; s[r][2 * i] = v.y; c[r][2 * i + 1] = v.z; s[r][2 * i + 1] = v.w;
+          }
+          if (MODE < 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s[r][i] = -s[r][i];
+          }
         }
       }
     }
-    for (int h0 = slot; h0 < H; h0 += kUnroll * HPI) {
+    for (int h0 = slot; h0 < H; h0 += UPR * HPI) {
       uint4 lo[kUnroll], hi[kUnroll];
       int64_t doff[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
-        const int h = h0 + u * HPI;
+        const int r = u / UPR;
+        const int h = h0 + (u % UPR) * HPI;
+        const int64_t t = tb + r;
         doff[u] = -1;
-        if (h < H) {
+        if (h < H && t < S_pad) {
           const int g = h / hp, j = h - g * hp;
-          const int64_t seq_off = (srow * H + h) * (int64_t)D;
+          const int64_t seq_off = (srow[r] * H + h) * (int64_t)D;
           const int64_t head_off = (((int64_t)g * S_pad + t) * hp + j) * (int64_t)D;
           const bf16* sp = src + (TO_HEAD ? seq_off : head_off);
           doff[u] = TO_HEAD ? head_off : seq_off;
           const int64_t so = (TO_HEAD ? seq_off : head_off) + 8 * sub;
-          if (pad_row || !usp::in_bounds(so, 8, n_src, status) ||
+          if (pad_row[r] || !usp::in_bounds(so, 8, n_src, status) ||
               !usp::in_bounds(so + D / 2, 8, n_src, status)) {
             lo[u] = make_uint4(0, 0, 0, 0);
             hi[u] = lo[u];
@@ -181,6 +193,7 @@ __global__ void __launch_bounds__(256) repack_kernel(
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         if (doff[u] < 0) continue;
+        const int r = u / UPR;
         uint4 a = lo[u], b = hi[u];
         if (MODE != 0) {
           const bf16* xa = reinterpret_cast<const bf16*>(&lo[u]);
@@ -192,12 +205,12 @@ __global__ void __launch_bounds__(256) repack_kernel(
             const float x1 = __bfloat162float(xa[i]);
             const float x2 = __bfloat162float(xb[i]);
             // IEEE fp32, each product rounded separately (no FMA contraction)
-            const float y1 = __fsub_rn(__fmul_rn(x1, c[i]), __fmul_rn(x2, s[i]));
-            const float y2 = __fadd_rn(__fmul_rn(x2, c[i]), __fmul_rn(x1, s[i]));
+            const float y1 = __fsub_rn(__fmul_rn(x1, c[r][i]), __fmul_rn(x2, s[r][i]));
+            const float y2 = __fadd_rn(__fmul_rn(x2, c[r][i]), __fmul_rn(x1, s[r][i]));
             ya[i] = __float2bfloat16_rn(y1);
             yb[i] = __float2bfloat16_rn(y2);
           }
-          if (zero_row) { a = make_uint4(0, 0, 0, 0); b = a; }
+          if (zero_row[r]) { a = make_uint4(0, 0, 0, 0); b = a; }
         }
         bf16* dp = dst + doff[u];
         if (usp::in_bounds(doff[u] + 8 * sub, 8, n_dst, status) &&
@@ -210,29 +223,43 @@ __global__ void __launch_bounds__(256) repack_kernel(
   }
 }
 
-int repack_grid(int64_t S_pad) {
-  int64_t blocks = (S_pad + 7) / 8;  // 8 warps (tokens) per block
+int repack_grid(int64_t S_pad, int rows_per_warp) {
+  int64_t blocks = (S_pad + 8 * rows_per_warp - 1) / (8 * rows_per_warp);  // 8 warps per block
   const int64_t cap = 152 * 64;      // grid-stride beyond this
   if (blocks > cap) blocks = cap;
   return (int)(blocks < 1 ? 1 : blocks);
 }
 
+template <int D, bool TO_HEAD, int R>
+cudaError_t launch_rows(int mode, const bf16* src, bf16* dst, const int32_t* pos,
+                        const float* cs, int64_t rope_len, int64_t S, int64_t S_pad, int H,
+                        int hp, unsigned* status, int64_t zz, int P, cudaStream_t st) {
+  const int grid = repack_grid(S_pad, R);
+  if (mode == 0)
+    repack_kernel<D, 0, TO_HEAD, R><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad,
+                                                          H, hp, status, zz, P);
+  else if (mode > 0)
+    repack_kernel<D, 1, TO_HEAD, R><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad,
+                                                          H, hp, status, zz, P);
+  else
+    repack_kernel<D, -1, TO_HEAD, R><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S,
+                                                           S_pad, H, hp, status, zz, P);
+  usp_count_launches(1);
+  return cudaGetLastError();
+}
+
+// Two rows per warp when one row's heads fill at most half of a warp's
+// load steps (H <= 2 * 32/(D/16)), one otherwise.
 template <int D, bool TO_HEAD>
 cudaError_t launch_mode(int mode, const bf16* src, bf16* dst, const int32_t* pos,
                         const float* cs, int64_t rope_len, int64_t S, int64_t S_pad, int H,
                         int hp, unsigned* status, int64_t zz, int P, cudaStream_t st) {
-  const int grid = repack_grid(S_pad);
-  if (mode == 0)
-    repack_kernel<D, 0, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad, H,
-                                                       hp, status, zz, P);
-  else if (mode > 0)
-    repack_kernel<D, 1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad, H,
-                                                       hp, status, zz, P);
-  else
-    repack_kernel<D, -1, TO_HEAD><<<grid, 256, 0, st>>>(src, dst, pos, cs, rope_len, S, S_pad,
-                                                        H, hp, status, zz, P);
-  usp_count_launches(1);
-  return cudaGetLastError();
+  constexpr int HPI = 32 / (D / 16);
+  if (H <= 2 * HPI)
+    return launch_rows<D, TO_HEAD, 2>(mode, src, dst, pos, cs, rope_len, S, S_pad, H, hp, status,
+                                      zz, P, st);
+  return launch_rows<D, TO_HEAD, 1>(mode, src, dst, pos, cs, rope_len, S, S_pad, H, hp, status,
+                                    zz, P, st);
 }
 
 }  // namespace
