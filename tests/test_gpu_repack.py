@@ -95,6 +95,10 @@ def test_seq_to_head_tiny(which, mode):
     (777, 4, 8, 4, 64, [0, 100, 101, 401, 777]),
     (30, 4, 8, 4, 128, None),
     (1, 8, 8, 8, 128, None),
+    # one shard, an odd number of rows: the few-head passes take two rows
+    # per warp and the last pair holds a single row
+    (777, 1, 4, 2, 128, None),
+    (255, 1, 2, 2, 64, [0, 100, 255]),
 ])
 def test_seq_to_head_small_ragged(case):
     for which, mode in (("q", 1), ("k", 1), ("v", 0)):
@@ -181,6 +185,23 @@ def test_head_to_seq_bit_exact(D, mode):
     pos, _ = O.positions_docs(S, P)
     xh = normal_bf16((P, S, H // P, D), 12, "do")
     out = torch.empty((S, H, D), dtype=torch.bfloat16, device="cuda")
+    B.usp_head_to_seq(d, to_dev(xh), H, torch.from_numpy(pos.astype(np.int32)).cuda(),
+                      torch.from_numpy(table).cuda(), S, mode, out)
+    torch.cuda.synchronize()
+    want = O.head_to_seq(xh)
+    if mode != 0:
+        want = O.rope_recipe_bf16(want, pos, table, inverse=mode < 0)
+    assert np.array_equal(to_bits(out), want)
+
+
+@pytest.mark.parametrize("D,mode", [(128, -1), (64, 0)])
+def test_head_to_seq_odd_rows_few_heads(D, mode):
+    S, P, H = 777, 1, 2            # two rows per warp, the last pair incomplete
+    d = _dims(S, P, H, H, D)
+    table = O.rope_table_f32(S, D, 1.0e4)
+    pos, _ = O.positions_docs(S, P)
+    xh = normal_bf16((P, S, H // P, D), 16, "do")
+    out = torch.full((S, H, D), 3.0, dtype=torch.bfloat16, device="cuda")
     B.usp_head_to_seq(d, to_dev(xh), H, torch.from_numpy(pos.astype(np.int32)).cuda(),
                       torch.from_numpy(table).cuda(), S, mode, out)
     torch.cuda.synchronize()
