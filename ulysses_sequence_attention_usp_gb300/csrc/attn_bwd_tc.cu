@@ -71,8 +71,9 @@ struct Bars {
   uint64_t ring_empty[4];  // per stage: the MMAs reading it completed
   uint64_t sd_full;       // dq: S and dP of the iteration computed; dkdv: S^T computed
   uint64_t dp_full;       // dkdv: dP^T computed
-  uint64_t consumed;      // dq: both elementwise groups read S and dP; dkdv: they read
-                          // dP^T (256 arrivals)
+  uint64_t consumed;      // dq: both elementwise groups read dP; dkdv: they read dP^T
+                          // (256 arrivals)
+  uint64_t s_consumed;    // dq: both elementwise groups read S (256 arrivals)
   uint64_t q_ready;       // dq: the Q tile is in TMEM (256 arrivals)
   uint64_t p_full[2];     // dkdv: P^T published ([0]), dS^T published ([1]);
                           // dq: dS written ([0]); 256 arrivals each
@@ -135,6 +136,7 @@ __device__ __forceinline__ void init_common(Bars* bars, int empty_count) {
   tc::mbar_init(&bars->sd_full, 1);
   tc::mbar_init(&bars->dp_full, 1);
   tc::mbar_init(&bars->consumed, 256);
+  tc::mbar_init(&bars->s_consumed, 256);
   tc::mbar_init(&bars->q_ready, 256);
   for (int b = 0; b < 2; ++b) {
     tc::mbar_init(&bars->p_full[b], 256);
@@ -284,9 +286,10 @@ __device__ __forceinline__ void mma_loop_dkdv(uint8_t* smem, Bars* bars, volatil
 // ring stage):
 //   S(j) = Q K_j^T (T0, TS),  dP(j) = dO V_j^T (T1, SS)
 //   dQ += dS(j) K_j   with dS(j) in TMEM columns R..R+63              (TS)
-// S(j+1) and dP(j+1) are issued as soon as the elementwise groups have read
-// S(j) and dP(j) ("consumed"), before they finish dS(j), so the tensor pipe
-// keeps working while they compute.  The dS columns are rewritten for j+1
+// S(j+1) is issued as soon as the elementwise groups have read S(j)
+// (`s_consumed`) and dP(j+1) as soon as they have read dP(j) (`consumed`),
+// before they finish dS(j), so the tensor pipe keeps working while they
+// read dP and compute.  The dS columns are rewritten for j+1
 // only after done[0] of dQ(j).  (Issuing dQ from a second warp was slower:
 // the two streams interleave their MMAs in the pipe.)
 template <int D>
@@ -321,12 +324,14 @@ __device__ __forceinline__ void mma_loop_dq(uint8_t* smem, Bars* bars, volatile 
   }
   for (int j = 0; ok && j < n_it; ++j) {
     const int st = j % C::NST2, s0 = 2 * st;
-    if (!(ok = tc::mbar_wait_warp(&bars->consumed, j & 1, abort))) break;
     if (j + 1 < n_it) {
       const int nst = (j + 1) % C::NST2, n0 = 2 * nst, n1 = 2 * nst + 1;
+      if (!(ok = tc::mbar_wait_warp(&bars->s_consumed, j & 1, abort))) break;
       if (!(ok = tc::mbar_wait_warp(&bars->ring_full[nst], ((j + 1) / C::NST2) & 1, abort))) break;
       tc::fence_after_sync();
       mma_tile_s_ts<D>(tmem + kDqT0, tmem + kDqQ, ring + n0 * C::TILE);
+      if (!(ok = tc::mbar_wait_warp(&bars->consumed, j & 1, abort))) break;
+      tc::fence_after_sync();
       mma_tile_ss<C>(tmem + kDqT1, fix, ring + n1 * C::TILE);
       tc::mma_commit_w(&bars->sd_full);
     }
@@ -439,7 +444,10 @@ __device__ __forceinline__ bool dq_half(uint32_t tS, uint32_t tP, uint32_t tR, i
                                         int hi, float nlse2, float ndl, float sl2, Bars* bars,
                                         int j, volatile int* abort) {
   uint32_t sv[64], dv[64];
-  tc::tmem_ld2_x64(tS + 64 * h, tP + 64 * h, sv, dv);
+  tc::tmem_ld_x64(tS + 64 * h, sv);
+  tc::fence_before_sync();
+  tc::mbar_arrive(&bars->s_consumed);      // S(j+1) may overwrite S now
+  tc::tmem_ld_x64(tP + 64 * h, dv);
   tc::fence_before_sync();
   tc::mbar_arrive(&bars->consumed);
   uint32_t w[32];
