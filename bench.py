@@ -241,6 +241,7 @@ def workload_config(args, wl, world=1):
             "shards": ("contiguous, K/V all-gather context parallelism"
                        if allgather else "zigzag" if args.zigzag else "contiguous"),
             "ring": args.ring,
+            "launch": "CUDA graph replay" if getattr(args, "graph", False) else "eager",
             "parallelism": (f"replicas x{world} (P={wl.P} virtual CP ranks per GPU)"
                             if allgather else
                             f"replicas x{world} (P={wl.P} virtual shards per GPU)")}
@@ -325,6 +326,9 @@ def run_usp(args, wl, inp):
     ua = make_pipeline()
     q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
     st = torch.cuda.current_stream(dev)
+    if args.graph:   # graph capture needs a stream other than the default one
+        st = torch.cuda.Stream(dev)
+        st.wait_stream(torch.cuda.current_stream(dev))
     d = ua.dims
     rows = getattr(ua, "S_pad", wl.S)          # rows of the sequence-layout buffers
     bq = rows * wl.Hq * wl.D * 2
@@ -408,6 +412,20 @@ def run_usp(args, wl, inp):
     for _ in range(args.warmup):
         step()
     ua.check(st)
+    graph, per_step = None, 0
+    if args.graph:   # one step's launches, recorded once and replayed
+        graph = torch.cuda.CUDAGraph()
+        n0 = B.usp_launch_count()
+        with torch.cuda.stream(st):
+            graph.capture_begin(capture_error_mode="thread_local")
+            try:
+                step()
+            finally:
+                graph.capture_end()
+        per_step = B.usp_launch_count() - n0
+        with torch.cuda.stream(st):
+            graph.replay()
+        ua.check(st)
 
     def barrier():
         if world > 1:
@@ -423,14 +441,24 @@ def run_usp(args, wl, inp):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(st)
-    for i in range(args.steps):
-        step(evs[i])
+    if graph is not None:
+        with torch.cuda.stream(st):
+            for i in range(args.steps):
+                graph.replay()
+    else:
+        for i in range(args.steps):
+            step(evs[i])
     t_end.record(st)
     barrier()
-    launches = B.usp_launch_count() - n0
+    launches = B.usp_launch_count() - n0 + per_step * (args.steps if graph is not None else 0)
     clk = clocks.stop()
     ua.check(st)
     elapsed = t_start.elapsed_time(t_end) / 1e3
+    if graph is not None:   # per-stage times from the same steps run eagerly
+        for i in range(args.steps):
+            step(evs[i])
+        barrier()
+        ua.check(st)
     stage_ms = {n: statistics.median(e[j].elapsed_time(e[j + 1]) for e in evs)
                 for j, n in enumerate(stage_names)}
     elapsed = reduce_max(elapsed, world, dev)
@@ -605,6 +633,9 @@ def main():
                     help="zigzag shard layout (rank r holds chunks r and 2P-1-r of 2P)")
     ap.add_argument("--ring", type=int, default=1,
                     help="ring steps of the forward (key windows merged by log-sum-exp)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one CUDA graph of the step (launch-bound small "
+                         "problems); per-stage times then come from eager steps")
     ap.add_argument("--cp", choices=["ulysses", "allgather"], default="ulysses",
                     help="sequence parallelism: Ulysses all-to-all (default) or context "
                          "parallelism with a K/V all-gather")

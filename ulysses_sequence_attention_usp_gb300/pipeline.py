@@ -44,7 +44,35 @@ def _check_input(name, t, rows, heads, D, device):
         raise ValueError(f"{name} must be contiguous")
 
 
-class UlyssesAttention:
+class _GraphStep:
+    """CUDA-graph capture of one step (forward + backward), shared by the
+    attention pipelines."""
+
+    def capture_step(self, q, k, v, do):
+        """Record one forward + backward of these input tensors into a CUDA
+        graph and return it (a torch.cuda.CUDAGraph): each replay() runs the
+        step's kernels again on the tensors' current contents, into the same
+        output buffers, without a host-side launch per kernel (small
+        problems are launch-bound).  One eager step runs first, so that the
+        library's modules are loaded and its kernel attributes set before
+        capture."""
+        dev = self.device
+        self.step(q, k, v, do)
+        torch.cuda.current_stream(dev).synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            graph.capture_begin(capture_error_mode="thread_local")
+            try:
+                self.step(q, k, v, do)
+            finally:
+                graph.capture_end()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        return graph
+
+
+class UlyssesAttention(_GraphStep):
     def __init__(self, S, P, Hq, Hkv, D, cu_seqlens=None, rope_base=1.0e4, yarn_factor=1.0,
                  yarn_orig_ctx=0, rope_len=0, scale=0.0, device="cuda", rope_table=None,
                  causal=True, zigzag=False, ring=1):
@@ -161,7 +189,7 @@ class UlyssesAttention:
         B.usp_device_status(stream)
 
 
-class AllGatherCPAttention:
+class AllGatherCPAttention(_GraphStep):
     """Context parallelism with a K/V all-gather over P virtual ranks
     (basetenlabs/Megatron-LM PR #7 "GLM-5.2 131k context parallelism",
     Purpose: the CP forward all-gathers the KV of every rank, the backward
