@@ -37,6 +37,7 @@ SMALL = [  # S, P, Hq, Hkv, D, doc lengths (None = one sequence)
     (600, 2, 16, 2, 128, [200, 400]),     # G = 8 as in the packed 64/8 workload
     (300, 2, 8, 2, 128, [100, 0, 150, 0, 50]),  # empty documents in cu_seqlens
     (512, 1, 4, 2, 64, [200, 312]),       # one rank (P = 1): no head split
+    (390, 2, 6, 2, 64, [130, 260]),       # G = 3: one query head per forward CTA, 3 slots
 ]
 
 
