@@ -141,6 +141,16 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def _query_once(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits"]
+        if self.bus_id:
+            cmd += ["-i", self.bus_id]
+        try:
+            out = subprocess.run(cmd, capture_output=True, text=True, timeout=30).stdout
+        except Exception:
+            return []
+        return [ln.strip() for ln in out.splitlines() if ln.strip()]
+
     def stop(self):
         if self.proc is None:
             return None
@@ -150,9 +160,19 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self._t.join(timeout=2)
+        res = self._summary(self.lines)
+        if res is None:   # the region ended before the first sample: read once right after
+            res = self._summary(self._query_once())
+            if res is not None:
+                res["samples"] = 0
+                res["note"] = "timed region shorter than one 200 ms sample; read right after it"
+        return res
+
+    @staticmethod
+    def _summary(lines):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue

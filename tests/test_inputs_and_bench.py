@@ -76,3 +76,14 @@ def test_both_arms_lines_share_the_config():
         assert gpu[k] == ref[k]
     src = open(bench.__file__).read()
     assert src.count("base_line(args, wl,") == 3      # the definition and one call per arm
+
+
+def test_clock_summary_parses_nvidia_smi_lines():
+    lines = ["1935, 2070, 1380.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "1965, 2070, 1390.1, 0x0000000000000000, Not Active, Not Active, Not Active, "
+             "Not Active",
+             "garbled"]
+    d = bench.ClockSampler._summary(lines)
+    assert d == {"sm_mhz": 1950.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                 "samples": 2}
+    assert bench.ClockSampler._summary([]) is None
