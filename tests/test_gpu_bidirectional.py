@@ -125,3 +125,39 @@ def test_bidirectional_full_size_packed_sampled():
         r_dk, r_dv = orc.dkv_keys(kh, keys, np.arange(a, b))
         check_grad(to_f64(ua.dk[a:a + 48, kh]), r_dk, "dk")
         check_grad(to_f64(ua.dv[a:a + 48, kh]), r_dv, "dv")
+
+
+def test_bidirectional_120k_sampled():
+    """The 120K SP8 workload (YaRN to 131072) in bidirectional mode, as
+    `bench.py --bidirectional` runs it: O, LSE and dQ on sampled rows of
+    three heads.  Every row sees all 120 000 keys, so each sampled row's
+    oracle values are one full row of fp64 attention."""
+    wl = WORKLOADS["sp8_120k"]
+    inp = make_inputs(wl, 0)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl, causal=False)
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                          rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
+                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len,
+                          causal=False, rope_table=orc.table())
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    ua.step(q, k, v, do)
+    ua.check()
+    rng = np.random.default_rng(7)
+    S = wl.S
+    rows = np.unique(np.concatenate([[0, 127, 128, 77824, S - 1], rng.integers(0, S, 6)]))
+    lse = ua.lse.reshape(wl.Hq, wl.S_pad)
+    heads = sorted({0, wl.Hq - 1, int(rng.integers(0, wl.Hq))})
+    got_o, ref_o, got_l, ref_l, got_dq, ref_dq = [], [], [], [], [], []
+    for h in heads:
+        r_o, r_l = orc.fwd_rows(h, rows)
+        got_o.append(to_f64(ua.o[rows, h]))
+        ref_o.append(r_o)
+        got_l.append(lse[h, rows].cpu().numpy().astype(np.float64))
+        ref_l.append(r_l)
+        got_dq.append(to_f64(ua.dq[rows, h]))
+        ref_dq.append(orc.dq_rows(h, rows))
+    check_o(np.concatenate(got_o), np.concatenate(ref_o))
+    check_grad(np.concatenate(got_dq), np.concatenate(ref_dq), "dq")
+    # 1e-3 against fp64 attention of the recipe-rotated bf16 Q, K
+    check_lse(np.concatenate(got_l), np.concatenate([orc.lse_rows_recipe(h, rows)
+                                                     for h in heads]))
