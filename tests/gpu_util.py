@@ -168,3 +168,39 @@ class SampledOracle:
         keys = np.arange(u_lo, u_hi)
         dk = O.rope_rotate(dk[:, None, :], self.pos[keys], self.cos, self.sin, inverse=True)[:, 0]
         return dk, dv
+
+
+def check_sampled_full_size(wl, inp, orc, o, lse, dq, dk, dv, seed, buf_of=None,
+                            tail_keys=True):
+    """Oracle checks of one full-size step on sampled rows: O, dQ and LSE
+    (1e-3 against the recipe-rotated bf16 Q, K) for three query heads, and
+    dK/dV of the last 48 keys of the sequence (or of the last document) for
+    the first and last KV heads.  o, dq, dk, dv are the sequence-layout
+    outputs ([rows][H][D] device tensors), lse the head-layout LSE
+    ([Hq][S_pad] after reshaping); buf_of maps a global row to its row in
+    the sequence-layout buffers (identity when None)."""
+    S = wl.S
+    rng = np.random.default_rng(seed)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, S // 2, S - 1], rng.integers(0, S, 8)]))
+    bo = (lambda r: r) if buf_of is None else (lambda r: buf_of[r])
+    heads = sorted({0, wl.Hq - 1, int(rng.integers(0, wl.Hq))})
+    got_o, ref_o, got_l, ref_l, got_dq, ref_dq = [], [], [], [], [], []
+    for h in heads:
+        r_o, _ = orc.fwd_rows(h, rows)
+        got_o.append(to_f64(o[bo(rows), h]))
+        ref_o.append(r_o)
+        got_l.append(lse[h, rows].cpu().numpy().astype(np.float64))
+        ref_l.append(orc.lse_rows_recipe(h, rows))
+        got_dq.append(to_f64(dq[bo(rows), h]))
+        ref_dq.append(orc.dq_rows(h, rows))
+    check_o(np.concatenate(got_o), np.concatenate(ref_o))
+    check_grad(np.concatenate(got_dq), np.concatenate(ref_dq), "dq")
+    check_lse(np.concatenate(got_l), np.concatenate(ref_l))
+    if tail_keys:
+        end = S if inp.cu is None else int(inp.cu[-1])
+        lo = end - 48
+        for kh in sorted({0, wl.Hkv - 1}):
+            r_dk, r_dv = orc.dkv_tail(kh, lo, end)
+            idx = bo(np.arange(lo, end))
+            check_grad(to_f64(dk[idx, kh]), r_dk, "dk")
+            check_grad(to_f64(dv[idx, kh]), r_dv, "dv")

@@ -11,9 +11,11 @@ import torch
 
 from oracle import usp_oracle as O
 from ulysses_sequence_attention_usp_gb300 import binding as B
+from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, make_inputs
 from ulysses_sequence_attention_usp_gb300.pipeline import UlyssesAttention
 
-from gpu_util import check_grad, check_lse, check_o, lse_tol_end_to_end, to_dev, to_f64
+from gpu_util import (SampledOracle, check_grad, check_lse, check_o, check_sampled_full_size,
+                      lse_tol_end_to_end, to_dev, to_f64)
 from test_gpu_attention import _kernel_inputs, _setup
 
 pytestmark = pytest.mark.gpu
@@ -120,3 +122,21 @@ def test_ring_pipeline_vs_full_sequence(case, R, causal):
     nq = np.linalg.norm(f(inp.q), axis=-1).max()
     nk = np.linalg.norm(f(inp.k), axis=-1).max()
     check_lse(lse, ref["lse"], lse_tol_end_to_end(nq, nk, 1.0 / math.sqrt(wl.D)))
+
+
+def test_ring_120k_sampled():
+    """The 120K SP8 workload with four ring steps, as `bench.py --ring 4`
+    runs it: sampled rows of O, LSE and dQ and the last 48 keys' dK/dV
+    against the oracle (the merged O and LSE feed the backward)."""
+    wl = WORKLOADS["sp8_120k"]
+    inp = make_inputs(wl, 0)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                          rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
+                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len,
+                          rope_table=orc.table(), ring=4)
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    dq, dk, dv = ua.step(q, k, v, do)
+    ua.check()
+    check_sampled_full_size(wl, inp, orc, ua.o, ua.lse.reshape(wl.Hq, wl.S_pad), dq, dk, dv,
+                            seed=9)

@@ -11,10 +11,12 @@ import torch
 
 from oracle import usp_oracle as O
 from ulysses_sequence_attention_usp_gb300 import binding as B
-from ulysses_sequence_attention_usp_gb300.inputs import cu_seqlens, normal_bf16
+from ulysses_sequence_attention_usp_gb300.inputs import (WORKLOADS, cu_seqlens, make_inputs,
+                                                        normal_bf16)
 from ulysses_sequence_attention_usp_gb300.pipeline import UlyssesAttention
 
-from gpu_util import check_grad, check_o, to_bits, to_dev, to_f64
+from gpu_util import (SampledOracle, check_grad, check_o, check_sampled_full_size, to_bits,
+                      to_dev, to_f64)
 from test_gpu_attention import _setup
 
 pytestmark = pytest.mark.gpu
@@ -92,3 +94,22 @@ def test_zigzag_pipeline_vs_full_sequence(case, causal):
     check_grad(glob(dv), ref["dv"], "dv")
     pad = inv[S:]
     assert not to_f64(ua.o)[pad].any() and not to_f64(dq)[pad].any()
+
+
+def test_zigzag_120k_sampled():
+    """The 120K SP8 workload in the zigzag shard layout, as `bench.py
+    --zigzag` runs it: sampled rows of O, LSE and dQ and the last 48 keys'
+    dK/dV against the oracle, read through the zigzag row map."""
+    wl = WORKLOADS["sp8_120k"]
+    inp = make_inputs(wl, 0)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                          rope_base=wl.rope_base, yarn_factor=wl.yarn_factor,
+                          yarn_orig_ctx=wl.yarn_orig_ctx, rope_len=wl.rope_len,
+                          rope_table=orc.table(), zigzag=True)
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    dq, dk, dv = ua.step(q, k, v, do)
+    ua.check()
+    inv = np.argsort(O.zigzag_order(ua.S_pad, wl.P))    # global row t -> buffer row
+    check_sampled_full_size(wl, inp, orc, ua.o, ua.lse.reshape(wl.Hq, ua.S_pad), dq, dk, dv,
+                            seed=8, buf_of=inv)
