@@ -33,6 +33,16 @@ SMALL_CASES = [
 ]
 
 
+# larger grids under the guards: the 8K pipeline (forward, both backward
+# passes, every permutation) and the 120K permutations on sampled rows,
+# including rows past the grid-stride threshold
+LARGE_CASES = [
+    "tests/test_gpu_attention.py::test_full_workload_sampled[qwen8k]",
+    "tests/test_gpu_repack.py::test_seq_to_head_120k_yarn_sampled_rows",
+    "tests/test_gpu_repack.py::test_head_to_seq_120k_sampled_rows",
+]
+
+
 def _child(args, timeout=1200):
     env = dict(os.environ, USP_DEBUG_BOUNDS="1")
     return subprocess.run([sys.executable] + args, cwd=ROOT, env=env, capture_output=True,
@@ -79,3 +89,11 @@ def test_guard_reports_out_of_range_document_id():
         B.usp_device_status()
     assert e.value.status == 6        # USP_ERR_OUT_OF_BOUNDS
     B.usp_device_status()             # reported once, then cleared
+
+
+def test_large_cases_run_clean_under_index_guards():
+    from ulysses_sequence_attention_usp_gb300 import build
+    build.build(debug=True)
+    r = _child(["-m", "pytest", "-q", "-m", "gpu", "-p", "no:cacheprovider", *LARGE_CASES])
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout and "skipped" not in r.stdout.splitlines()[-1]
