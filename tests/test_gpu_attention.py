@@ -22,8 +22,8 @@ from ulysses_sequence_attention_usp_gb300 import binding as B
 from ulysses_sequence_attention_usp_gb300.inputs import WORKLOADS, custom_workload, make_inputs
 from ulysses_sequence_attention_usp_gb300.pipeline import UlyssesAttention
 
-from gpu_util import (SampledOracle, check_grad, check_lse, check_o, lse_tol_end_to_end,
-                      to_bits, to_dev, to_f64)
+from gpu_util import (SampledOracle, check_grad, check_lse, check_o, check_sampled_full_size,
+                      lse_tol_end_to_end, to_bits, to_dev, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -282,3 +282,27 @@ def test_full_workload_first_keys(name):
         r_dk, r_dv = orc.dkv_keys(kh, keys, np.arange(a, e))
         check_grad(to_f64(ua.dk[a:a + 48, kh]), r_dk, "dk")
         check_grad(to_f64(ua.dv[a:a + 48, kh]), r_dv, "dv")
+
+
+def test_d64_long_packed_sampled():
+    """Head dimension 64 at 16K packed tokens (many tiles, long key-stationary
+    loops, documents straddling shards), sampled against the oracle: the
+    D = 64 kernels otherwise run only at small sizes."""
+    lens = [5000, 129, 1, 7000, 4254]
+    wl = custom_workload(16384, 4, 16, 4, 64, base=1.0e4, thd_lens=lens)
+    inp = make_inputs(wl, 3, lens=lens)
+    orc = SampledOracle(inp.q, inp.k, inp.v, inp.do, inp.cu, wl)
+    ua = UlyssesAttention(wl.S, wl.P, wl.Hq, wl.Hkv, wl.D, cu_seqlens=inp.cu,
+                          rope_base=wl.rope_base, rope_table=orc.table())
+    q, k, v, do = (to_dev(x) for x in (inp.q, inp.k, inp.v, inp.do))
+    dq, dk, dv = ua.step(q, k, v, do)
+    ua.check()
+    check_sampled_full_size(wl, inp, orc, ua.o, ua.lse.reshape(wl.Hq, wl.S_pad), dq, dk, dv,
+                            seed=11)
+    # dK/dV of the first 48 keys of the longest document (7000 rows)
+    a, e = int(inp.cu[3]), int(inp.cu[4])
+    keys = np.arange(a, a + 48)
+    for kh in (0, wl.Hkv - 1):
+        r_dk, r_dv = orc.dkv_keys(kh, keys, np.arange(a, e))
+        check_grad(to_f64(dk[a:a + 48, kh]), r_dk, "dk")
+        check_grad(to_f64(dv[a:a + 48, kh]), r_dv, "dv")
