@@ -200,11 +200,11 @@ def gpu_bus_id(torch):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample(wl, inp, target_s, fixed_rows=None, causal=True):
+def oracle_sample(wl, inp, target_s, fixed_rows=None, causal=True, keep=False):
     """Time the oracle's forward+backward of query head 0 (and its KV head)
     on the first S' rows, S' grown until one run takes about target_s
     seconds (or S' = fixed_rows).  Returns (seconds, S', scale factor to the
-    full workload)."""
+    full workload), and with keep=True also the last run's results."""
     from oracle import usp_oracle as O
     D = wl.D
     scale = 1.0 / math.sqrt(D)
@@ -221,7 +221,7 @@ def oracle_sample(wl, inp, target_s, fixed_rows=None, causal=True):
         if inp.cu is not None:
             cu = np.concatenate([inp.cu[inp.cu < Sp], [Sp]]).astype(np.int64)
         t0 = time.perf_counter()
-        O.full_sequence(q, k, v, do, cu, cos, sin, scale, causal)
+        res = O.full_sequence(q, k, v, do, cu, cos, sin, scale, causal)
         dt = time.perf_counter() - t0
         if fixed_rows or dt >= target_s / 3 or Sp >= wl.S:
             break
@@ -229,7 +229,29 @@ def oracle_sample(wl, inp, target_s, fixed_rows=None, causal=True):
     pairs_s = attended_pairs(Sp, cu, causal)
     pairs_f = attended_pairs(wl.S, inp.cu, causal)
     factor = (pairs_f * wl.Hq) / pairs_s
-    return dt, Sp, factor
+    return (dt, Sp, factor, res) if keep else (dt, Sp, factor)
+
+
+def parity_sample(ua, wl, ref, Sp):
+    """The GPU step's O, LSE and dQ of query head 0 on rows [0, S') against
+    the oracle run of the CPU-baseline leg.  With causal attention those rows
+    see only keys below S', so the oracle's values there are the full
+    problem's; the oracle rotates exactly in fp64, the GPU by the fp32 table
+    into bf16, so LSE differs by the rounding of the rotated Q, K."""
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    o, dq = f(ua.o[:Sp, 0]), f(ua.dq[:Sp, 0])
+    lse = ua.lse.reshape(wl.Hq, -1)[0, :Sp].cpu().numpy().astype(np.float64)
+    ro, rdq, rl = ref["o"][:, 0], ref["dq"][:, 0], ref["lse"][0]
+    d_o, d_dq = np.abs(o - ro), np.abs(dq - rdq)
+    fin = np.isfinite(rl)
+    res = {"sample": f"query head 0, rows [0, {Sp}) of the timed workload",
+           "o_max_abs": float(d_o.max()), "o_mean_abs": float(d_o.mean()),
+           "dq_max_rel": float(d_dq.max() / max(float(np.abs(rdq).max()), 1e-30)),
+           "lse_max_abs": float(np.abs(lse[fin] - rl[fin]).max()) if fin.any() else 0.0,
+           "criteria": {"o_max_abs": 2e-2, "o_mean_abs": 2e-3, "dq_max_rel": 5e-2}}
+    res["within_criteria"] = (res["o_max_abs"] <= 2e-2 and res["o_mean_abs"] <= 2e-3
+                              and res["dq_max_rel"] <= 5e-2)
+    return res
 
 
 def cpu_cores():
@@ -625,12 +647,17 @@ def run_usp(args, wl, inp):
             "clocks": clk,
         })
         if world == 1 and not args.no_cpu_baseline:
-            dt, Sp, factor = oracle_sample(wl, inp, args.cpu_seconds, causal=causal)
+            dt, Sp, factor, ref = oracle_sample(wl, inp, args.cpu_seconds, causal=causal,
+                                                keep=True)
             line["cpu_baseline"] = {
                 "value": wl.S / (dt * factor), "unit": "tokens/s", "cores": cpu_cores(),
                 "kind": "oracle",
                 "sample": (f"oracle fwd+bwd of q head 0 / kv head 0 on the first {Sp} rows "
                            f"({dt:.1f} s), scaled by attended pairs x heads ({factor:.4g}x)")}
+            # the same oracle run against the GPU's outputs on those rows (rows
+            # in sequence order: not for the zigzag layout; causal only)
+            if causal and not args.zigzag:
+                line["parity"] = parity_sample(ua, wl, ref, Sp)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

@@ -87,3 +87,24 @@ def test_clock_summary_parses_nvidia_smi_lines():
     assert d == {"sm_mhz": 1950.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
                  "samples": 2}
     assert bench.ClockSampler._summary([]) is None
+
+
+def test_parity_sample_reports_maxima():
+    import types
+    import torch
+    Sp, D = 5, 4
+    rng = np.random.default_rng(0)
+    ref = {"o": rng.standard_normal((Sp, 1, D)), "dq": rng.standard_normal((Sp, 1, D)),
+           "lse": rng.standard_normal((1, Sp))}
+    o = np.zeros((8, 2, D))
+    o[:Sp, 0] = ref["o"][:, 0] + 0.01
+    dq = np.zeros((8, 2, D))
+    dq[:Sp, 0] = ref["dq"][:, 0] * 1.02
+    lse = np.zeros((1, 2, 8))
+    lse[0, 0, :Sp] = ref["lse"][0] - 3e-4
+    ua = types.SimpleNamespace(o=torch.tensor(o), dq=torch.tensor(dq), lse=torch.tensor(lse))
+    r = bench.parity_sample(ua, types.SimpleNamespace(Hq=2), ref, Sp)
+    assert abs(r["o_max_abs"] - 0.01) < 1e-6 and abs(r["o_mean_abs"] - 0.01) < 1e-6
+    assert abs(r["dq_max_rel"] - 0.02) < 1e-6
+    assert abs(r["lse_max_abs"] - 3e-4) < 1e-6
+    assert r["within_criteria"] is False          # mean |dO| 1e-2 > 2e-3
