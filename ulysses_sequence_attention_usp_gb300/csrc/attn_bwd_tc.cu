@@ -787,7 +787,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------ delta = rowsum(dO*O)
-// One warp per (row, head): 16-byte loads, fp32 products and a shuffle sum.
+// D/8 lanes per (row, head): 16-byte loads, fp32 products and a shuffle sum;
+// a warp takes 32/(D/8) rows at a time, four such groups per step.
 // Writes both negated: ndelta = -delta and nlse2 = -LSE*log2(e) (-inf where
 // LSE = -inf).  Both arrays have rows of S_ws >= S_pad entries; entries
 // [S_pad, S_ws) get ndelta 0 and nlse2 -inf.
@@ -817,14 +818,28 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
   const int lane = threadIdx.x & 31;
   const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t base = w0 * RPW; base < n_rows; base += nw * RPW) {
-    const int64_t row = base + lane / LPR;    // row = (g*S_pad + t)*hq + j
-    float s = 0.f;
-    if (row < n_rows && usp::in_bounds(row * D + 8 * (lane % LPR), 8, n_rows * D, status)) {
-      const uint4 a = __ldcs(reinterpret_cast<const uint4*>(o + row * D) + lane % LPR);
-      const uint4 b = __ldcs(reinterpret_cast<const uint4*>(dout + row * D) + lane % LPR);
-      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+  // U row groups per warp step: the loads of all of them are issued before
+  // any is used, so each lane keeps 2*U 16-byte loads in flight
+  constexpr int U = 4;
+  for (int64_t base = w0 * RPW * U; base < n_rows; base += nw * RPW * U) {
+    uint4 a[U], b[U];
+    int64_t row[U];
+    bool ok[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      row[u] = base + u * RPW + lane / LPR;   // row = (g*S_pad + t)*hq + j
+      ok[u] = row[u] < n_rows &&
+              usp::in_bounds(row[u] * D + 8 * (lane % LPR), 8, n_rows * D, status);
+      a[u] = ok[u] ? __ldcs(reinterpret_cast<const uint4*>(o + row[u] * D) + lane % LPR)
+                   : make_uint4(0, 0, 0, 0);
+      b[u] = ok[u] ? __ldcs(reinterpret_cast<const uint4*>(dout + row[u] * D) + lane % LPR)
+                   : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float s = 0.f;
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b[u]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 fa = __bfloat1622float2(pa[i]);
@@ -832,19 +847,20 @@ __global__ void __launch_bounds__(256) delta_kernel(const bf16* __restrict__ o,
         s = fmaf(fa.x, fb.x, s);
         s = fmaf(fa.y, fb.y, s);
       }
-    }
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (row < n_rows && lane % LPR == 0) {
-      const int64_t gt = row / hq;
-      const int j = (int)(row - gt * hq);
-      const int64_t g = gt / S_pad, t = gt - g * S_pad;
-      const int64_t li = (g * hq + j) * S_ws + t;
-      const int64_t lj = (g * hq + j) * S_pad + t;
-      if (!usp::in_bounds(li, 1, n_ws, status) || !usp::in_bounds(lj, 1, n_rows, status)) continue;
-      delta[li] = -s;
-      const float x = lse[lj];
-      lse2[li] = x == -INFINITY ? -INFINITY : -(x * kLog2e);
+      for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      if (row[u] < n_rows && lane % LPR == 0) {
+        const int64_t gt = row[u] / hq;
+        const int j = (int)(row[u] - gt * hq);
+        const int64_t g = gt / S_pad, t = gt - g * S_pad;
+        const int64_t li = (g * hq + j) * S_ws + t;
+        const int64_t lj = (g * hq + j) * S_pad + t;
+        if (usp::in_bounds(li, 1, n_ws, status) && usp::in_bounds(lj, 1, n_rows, status)) {
+          delta[li] = -s;
+          const float x = lse[lj];
+          lse2[li] = x == -INFINITY ? -INFINITY : -(x * kLog2e);
+        }
+      }
     }
   }
 }
